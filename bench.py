@@ -1,0 +1,460 @@
+#!/usr/bin/env python3
+"""Benchmark: causal bf16 prefill TFLOP/s (B4 H32 S2048 D128) and decode HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one attn_fwd call on the prefill workload (the headline `value`),
+timed with CUDA events on the launching stream, L2 flushed between steps
+outside the events.  The decode workload (B64 H32 D128, cache padded to 8192,
+lengths uniform on [4096, 8192]) is timed the same way and reported under
+"decode".  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU checker (the only reference this method
+has) on a bounded sample of the same workload, on the host cores.
+
+Under torchrun (N > 1) each rank runs its own shard of the global batch
+(sequences are independent problems: no data-path collective); the process
+group carries only a barrier and the max over ranks of the timings.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from transformer_scaled_dot_fwd_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "causal attn fwd TFLOP/s (B4 H32 S2048 D128 bf16) and % peak; decode HBM GB/s"
+L2_FLUSH_BYTES = 256 << 20   # > the 129 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- counting
+
+def prefill_flops(B, H, Sq, Skv, D, causal):
+    """4*B*H*Sq*Skv*D (scores and weights @ V), halved for causal."""
+    f = 4.0 * B * H * Sq * Skv * D
+    return f / 2.0 if causal else f
+
+
+def decode_bytes(H, D, kv_len, elem=2):
+    """K and V bytes a decode step must read: sum_b 2*H*L_b*D*elem."""
+    return float(sum(2.0 * H * float(L) * D * elem for L in kv_len))
+
+
+def decode_flops(H, D, kv_len):
+    return float(sum(4.0 * H * float(L) * D for L in kv_len))
+
+
+# ----------------------------------------------------------------------------- environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(dist, x, device):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- timing
+
+def time_steps(fn, steps, stream, flush):
+    """Run fn() `steps` times; CUDA events on `stream` around each call, L2
+    flushed between calls outside the events.  Returns per-step ms."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for s in range(steps):
+        flush()
+        starts[s].record(stream)
+        fn()
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for f in ("prefill_tc.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "transformer_scaled_dot_fwd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_src = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (m_src and m_b) or m_src.group(1) != kernel_source_digest():
+        return None
+    return float(m_b.group(1))
+
+
+# ----------------------------------------------------------------------------- CPU checker timing
+
+def cpu_oracle_sample(q, k, v, w, kv_len, budget_s, rng_seed=0):
+    """Time the fp64 checker on a random sample of rows of the workload; the
+    sample is sized from a short calibration run to take about budget_s.
+    Returns (TFLOP/s, description, threads)."""
+    import oracle
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    kv_host = None if kv_len is None else kv_len.cpu().numpy()
+    rng = np.random.default_rng(rng_seed)
+
+    def rows_and_flops(n):
+        b = rng.integers(0, w.B, n)
+        h = rng.integers(0, w.H, n)
+        i = rng.integers(0, w.S, n)
+        vis = (i + 1) if w.causal else np.full(n, w.S)
+        if kv_host is not None:
+            L = kv_host[b]
+            vis = np.where(i < L, np.minimum(vis, L), 0)
+        return np.stack([b, h, i], 1), float(np.sum(4.0 * w.D * vis))
+
+    rows, _ = rows_and_flops(256)
+    t0 = time.perf_counter()
+    oracle.attention_rows(qc, kc, vc, rows, scale=w.softmax_scale, causal=w.causal, kv_len=kv_host)
+    per_row = max((time.perf_counter() - t0) / 256, 1e-7)
+    n = int(min(max(budget_s / per_row, 256), w.B * w.H * w.S))
+    rows, flops = rows_and_flops(n)
+    t0 = time.perf_counter()
+    oracle.attention_rows(qc, kc, vc, rows, scale=w.softmax_scale, causal=w.causal, kv_len=kv_host)
+    dt = time.perf_counter() - t0
+    desc = (f"{n} random query rows of the {w.name} workload ({flops / 1e9:.2f} GFLOP "
+            f"of the method's count), fp64, {dt:.1f} s")
+    return flops / dt / 1e12, desc, threads, dt
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = wl.PREFILL
+    q, k, v, kv_len = wl.prefill_inputs(w, device="cpu")
+    per_step = max(2.0, min(10.0, 150.0 / max(args.steps + args.warmup, 1)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(q, k, v, w, kv_len, per_step / 4)
+    vals, times, desc, threads = [], [], "", 0
+    for s in range(args.steps):
+        tf, desc, threads, dt = cpu_oracle_sample(q, k, v, w, kv_len, per_step, rng_seed=s + 1)
+        vals.append(tf)
+        times.append(dt)
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": float(np.mean(times) * 1e3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1), bf16-rounded inputs)",
+        "config": config_dict(w, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w, world):
+    return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
+            "global_batch": w.B * world, "seq_len": w.S,
+            "parallelism": f"dp{world} (independent sequences per GPU, no collective)" if world > 1 else "single GPU",
+            "l2": "flushed between steps (256 MB write), outside the timed events",
+            "timing": "CUDA events on the launching stream around each call; sum over steps; max over ranks"}
+
+
+def run_ours(args):
+    import transformer_scaled_dot_fwd_gb300 as attn
+    from transformer_scaled_dot_fwd_gb300 import build as _build
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    if rank == 0 or world == 1:
+        _build.build(quiet=True)
+    barrier(dist, device)
+    attn.lib()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    peaks, peak_src = load_peaks()
+
+    # -------------------------------------------------------------- prefill (headline)
+    w = wl.PREFILL
+    if args.only == "decode":
+        return run_decode_only(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
+    q, k, v, kv_len = wl.prefill_inputs(w, device=device, seed=w.seed + 1000 * rank)
+    out = torch.empty_like(q)
+
+    def step():
+        attn.attn_fwd(q, k, v, out=out, scale=w.softmax_scale, causal=w.causal, kv_len=kv_len)
+
+    for _ in range(args.warmup):
+        step()
+    attn.attn_device_status()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    sampler.start()
+    wall0 = time.perf_counter()
+    ms = time_steps(step, args.steps, stream, flush)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    barrier(dist, device)
+    attn.attn_device_status()
+    total_ms = max_over_ranks(dist, float(sum(ms)), device)
+    flops_step = prefill_flops(w.B, w.H, w.S, w.S, w.D, w.causal)
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    avg_ms = float(sum(ms)) / args.steps
+    achieved = flops_step / (avg_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    traffic = profiled_traffic("prefill_tc_B4H32S2048D128.md")
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense (burst: the kernel is timed alone)",
+                "kernel": "prefill_tc_kernel<128>",
+                "algorithmic_flops_per_launch": flops_step}
+
+    # -------------------------------------------------------------- decode
+    decode = None if args.only == "prefill" else decode_leg(args, attn, device, stream, flush, peaks,
+                                                            peak_src, world, rank, dist)
+    e2e = None if args.no_e2e else e2e_leg(args, attn, q, k, v, out, w, flops_step, world, dist, device)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, desc, threads, _ = cpu_oracle_sample(q, k, v, w, kv_len, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16)",
+        "config": config_dict(w, world),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+        "clocks": clocks, "gpu_launches": args.steps,
+        "wall_s_timed_region": wall, "kernel_source_digest": kernel_source_digest(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
+    dwk = wl.DECODE
+    if args.decode_batch:
+        dwk = wl.DecodeWorkload(dwk.name.replace("B64", f"B{args.decode_batch}"), args.decode_batch,
+                                dwk.H, dwk.Skv, dwk.D, dwk.seed, dwk.kv_len_range)
+    dq, dk, dv, dkl = wl.decode_inputs(dwk, device=device, seed=dwk.seed + 1000 * rank)
+    dout = torch.empty_like(dq)
+
+    def dstep():
+        attn.attn_decode(dq, dk, dv, out=dout, kv_len=dkl)
+
+    for _ in range(args.warmup):
+        dstep()
+    attn.attn_device_status()
+    dms = time_steps(dstep, args.steps, stream, flush)
+    attn.attn_device_status()
+    dtotal = max_over_ranks(dist, float(sum(dms)), device)
+    dbytes = decode_bytes(dwk.H, dwk.D, dkl.cpu().tolist())
+    d_avg = float(sum(dms)) / args.steps
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    d_gbs = dbytes / (d_avg * 1e-3) / 1e9
+    decode = {
+        "workload": dwk.name, "value": world * dbytes * args.steps / (dtotal * 1e-3) / 1e9,
+        "unit": "GB/s", "ms_per_step": d_avg,
+        "tflops": decode_flops(dwk.H, dwk.D, dkl.cpu().tolist()) / (d_avg * 1e-3) / 1e12,
+        "splits_per_head": attn.attn_decode_splits(dwk.B, dwk.H, dwk.Skv, dwk.D),
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": d_gbs / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "algorithmic_bytes_per_launch": dbytes},
+    }
+    del dq, dk, dv, dout
+    return decode
+
+
+def run_decode_only(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
+    decode = decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
+    if rank == 0:
+        print(json.dumps({"decode": decode}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_leg(args, attn, q, k, v, out, w, flops_step, world, dist, device):
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hout = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    dq2, dk2, dv2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq2.copy_(hq, non_blocking=True)
+        dk2.copy_(hk, non_blocking=True)
+        dv2.copy_(hv, non_blocking=True)
+        attn.attn_fwd(dq2, dk2, dv2, out=out, scale=w.softmax_scale, causal=w.causal)
+        hout.copy_(out, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, device)
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = out.numel() * out.element_size()
+    e2e = {"value": world * flops_step * e2e_steps / e2e_s / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "timing": "wall clock around pinned-host copies in, attn_fwd, copy out; synchronized"}
+    del hq, hk, hv, hout, dq2, dk2, dv2
+    return e2e
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="approximate CPU time of the fp64 checker baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="profiling runs: time one kernel family only")
+    ap.add_argument("--decode-batch", type=int, default=None,
+                    help="profiling runs: smaller decode batch than the workload's 64")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

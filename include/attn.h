@@ -1,0 +1,149 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) scaled dot-product attention library.
+ *
+ * The library computes multi-head scaled dot-product attention forward,
+ *
+ *     out = softmax(Q K^T * scale + M) V        independently per (batch, head),
+ *
+ * where M is 0 for an allowed (query, key) pair and -inf for a forbidden one,
+ * applied before the softmax.  The definition is the one shared by the pages
+ * "Attention from First Principles" (section 1, "In one line"; section 4,
+ * "Tiny example"), "Self-Attention" ("Scaled Dot-Product Attention", "Causal
+ * Masking") and "Attention from Scratch" (kube-dojo), Parts 2 and 3.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.   Tensors are dense, row-major (B, H, S, D) arrays with D fastest:
+ *           element (b, h, s, d) lives at ((b*H + h)*S + s)*D + d.  This is
+ *           the head-split layout of "Attention from scratch"
+ *           (open-llm-engineering), split_heads.  Decode tensors q and out are
+ *           (B, H, D), i.e. (B, H, 1, D).
+ * Memory.   Every tensor pointer is DEVICE memory owned by the caller, aligned
+ *           to 16 bytes (a pointer to an empty tensor may be NULL).  The
+ *           library never frees or retains it.  kv_len, when
+ *           not NULL, is a DEVICE array of B int32 values; it is read by the
+ *           kernels (no host synchronisation), and each value is clamped to
+ *           [0, Skv].
+ * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *           Calls are asynchronous: they enqueue work and return.  Argument
+ *           errors are detected on the host before anything is enqueued.
+ * dtype.    ATTN_BF16: bfloat16 inputs and output, fp32 accumulation and
+ *           softmax statistics, output rounded to nearest even.
+ *           ATTN_F32: float32 everywhere (no TF32).  Output dtype = input dtype.
+ * Masking.  causal: key j is visible from query i iff j <= i + (Skv - Sq)
+ *           (the last query is aligned with the last key; for Sq == Skv this
+ *           is the lower-triangular mask of the pages).  kv_len: keys
+ *           j >= kv_len[b] are masked (right padding, "Attention from Scratch"
+ *           (kube-dojo), Part 3 padding mask).  A query row that sees no key
+ *           outputs exact zeros (the pages raise an error for such a row; an
+ *           error cannot be raised per row from a batched kernel).
+ * Errors.   Every entry point returns ATTN_OK (0) or a negative code; on error
+ *           attn_last_error() (per calling thread) describes it.  Nothing is
+ *           printed and nothing aborts.
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#include <stdint.h>
+
+#if defined(_WIN32)
+#define ATTN_API
+#else
+#define ATTN_API __attribute__((visibility("default")))
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. */
+#define ATTN_F32 0
+#define ATTN_BF16 1
+
+/* Status codes. */
+#define ATTN_OK 0
+#define ATTN_EINVAL (-1)       /* bad argument: NULL pointer, bad size, misalignment, ... */
+#define ATTN_EUNSUPPORTED (-2) /* valid request this library does not implement (never a silent fallback) */
+#define ATTN_ECUDA (-3)        /* a CUDA runtime or driver call failed; see attn_last_error() */
+#define ATTN_ENOMEM (-4)       /* workspace allocation failed */
+#define ATTN_ETIMEOUT (-5)     /* a device-side wait hit its iteration limit (reported by attn_device_status) */
+
+/*
+ * attn_fwd -- prefill attention for a batch of multi-head sequences.
+ *
+ * Defines: "Attention from First Principles", section 5 "The full
+ * multi-head computation" (scores, scale by 1/sqrt(d_head), causal mask,
+ * softmax over keys, weights @ V), with the key-padding mask of "Attention
+ * from Scratch" (kube-dojo), Part 3, combined by logical AND.
+ *
+ *   q    (B, H, Sq,  D)  query rows
+ *   k    (B, H, Skv, D)  key rows
+ *   v    (B, H, Skv, D)  value rows
+ *   out  (B, H, Sq,  D)  written; must not overlap q, k or v
+ *   scale   multiplier of Q K^T; must be finite and >= 0 (1/sqrt(D) is the
+ *           pages' choice, "Why divide by the square root of the head
+ *           dimension?")
+ *   causal  0 or 1; causal with Sq > Skv is rejected (ATTN_EINVAL)
+ *   kv_len  NULL, or device int32[B]: per-sequence valid length.  With
+ *           kv_len the call is self-attention over a right-padded batch and
+ *           needs Sq == Skv; query rows i >= kv_len[b] output zeros.
+ *   dtype   ATTN_BF16: D must be 64 or 128.  ATTN_F32: D must be 64 or 128.
+ *
+ * Sizes: B, H >= 1; Sq, Skv >= 0 (an empty call returns ATTN_OK and does
+ * nothing); D as above; B*H*max(Sq,Skv)*D must fit in 2^31 rows of D.
+ */
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
+                      int Sq, int Skv, int D, float scale, int causal, const int32_t *kv_len,
+                      int dtype, void *stream);
+
+/*
+ * attn_decode -- one new query per (batch, head) against a KV cache.
+ *
+ * Defines: "Attention from First Principles", section 6 "Under the hood"
+ * (decode is a matrix-vector product against the whole cache) and "Scaled
+ * dot-product attention with masking", "Adding the causal mask" (with
+ * seq_q = 1 the query attends to every cached position, no mask).  The
+ * scale is 1/sqrt(D).
+ *
+ *   q       (B, H, D)        the new queries
+ *   kcache  (B, H, Skv, D)   cached keys, padded to Skv
+ *   vcache  (B, H, Skv, D)   cached values, padded to Skv
+ *   out     (B, H, D)        written
+ *   kv_len  NULL (every sequence uses all Skv positions) or device int32[B];
+ *           keys j >= kv_len[b] are ignored, kv_len[b] == 0 gives zeros.
+ *   dtype   ATTN_BF16 only; D must be 64 or 128.
+ *
+ * The kernel splits each sequence's keys into chunks processed in parallel
+ * and merges the partial softmax results; the partials live in a workspace
+ * the library allocates on first use (and grows when a call needs more),
+ * which attn_release() frees.  The workspace is shared by all calls on a
+ * device: calls that overlap in time on different streams of one device race.
+ */
+ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, void *out, int B,
+                         int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream);
+
+/*
+ * attn_decode_splits -- number of KV chunks attn_decode uses per (batch,
+ * head) for these sizes (for benchmarks and tests); negative on bad sizes.
+ */
+ATTN_API int attn_decode_splits(int B, int H, int Skv, int D);
+
+/*
+ * attn_device_status -- synchronise `stream`, then report and clear the
+ * device-side status word.  Returns ATTN_OK, ATTN_ETIMEOUT when a kernel gave
+ * up on a device-side wait (its output is then undefined), or ATTN_ECUDA when
+ * the synchronisation itself failed.
+ */
+ATTN_API int attn_device_status(void *stream);
+
+/* Description of the last error on the calling thread ("" if none). */
+ATTN_API const char *attn_last_error(void);
+
+/* Free library-owned device memory (decode workspace) on the current device. */
+ATTN_API void attn_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

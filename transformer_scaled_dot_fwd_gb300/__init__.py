@@ -1,0 +1,199 @@
+"""GB300 (sm_103a) scaled dot-product attention forward: Python binding.
+
+This module only marshals arguments to the C ABI declared in include/attn.h
+(``libattn.so`` next to this file): every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and streams.  There is
+no CPU path: when the library is missing, every call raises.
+
+    attn_fwd(q, k, v, out=None, scale=None, causal=False, kv_len=None, stream=None)
+    attn_decode(q, kcache, vcache, out=None, kv_len=None, stream=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+ATTN_F32 = 0
+ATTN_BF16 = 1
+
+ATTN_OK = 0
+ATTN_EINVAL = -1
+ATTN_EUNSUPPORTED = -2
+ATTN_ECUDA = -3
+ATTN_ENOMEM = -4
+ATTN_ETIMEOUT = -5
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+# The exported functions, as declared in include/attn.h: name -> (restype, argtypes)
+_vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "attn_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
+    "attn_decode_splits": (_i, [_i, _i, _i, _i]),
+    "attn_device_status": (_i, [_vp]),
+    "attn_last_error": (ctypes.c_char_p, []),
+    "attn_release": (None, []),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero status from the library; ``code`` is the ATTN_E* value."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+def lib(path: Optional[str] = None):
+    """The loaded C library (ctypes handle with typed signatures)."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built; run `python -m transformer_scaled_dot_fwd_gb300.build`")
+        _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def _bind(handle):
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
+def attn_last_error() -> str:
+    return (lib().attn_last_error() or b"").decode(errors="replace")
+
+
+def _check(rc: int):
+    if rc != ATTN_OK:
+        raise AttnError(rc, attn_last_error())
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"unsupported dtype {t.dtype} (bfloat16 or float32)")
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check_tensor(name, t, ndim):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D")
+
+
+def _kv_len_arg(kv_len, B, device):
+    torch = _torch()
+    if kv_len is None:
+        return None
+    if not (kv_len.is_cuda and kv_len.dtype == torch.int32 and kv_len.shape == (B,)
+            and kv_len.is_contiguous() and kv_len.device == device):
+        raise ValueError("kv_len must be a contiguous int32 CUDA tensor of shape (B,) on q's device")
+    return kv_len
+
+
+def attn_fwd(q, k, v, out=None, scale: Optional[float] = None, causal: bool = False,
+             kv_len=None, stream=None):
+    """Prefill attention of (B, H, Sq, D) queries against (B, H, Skv, D) keys/values.
+
+    Returns ``out`` (allocated like q when not given).  See include/attn.h.
+    """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, 4)
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    if tuple(k.shape) != (B, H, Skv, D) or tuple(v.shape) != (B, H, Skv, D):
+        raise ValueError("k and v must be (B, H, Skv, D) matching q")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if out is None:
+        out = _torch().empty_like(q)
+    _check_tensor("out", out, 4)
+    if tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype:
+        raise ValueError("out must match q's shape and dtype")
+    kl = _kv_len_arg(kv_len, B, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Sq, Skv, D, float(scale),
+                        int(bool(causal)), _ptr(kl), _dtype_code(q), _stream_handle(stream))
+    _check(rc)
+    return out
+
+
+def attn_decode(q, kcache, vcache, out=None, kv_len=None, stream=None):
+    """One query per (batch, head): q (B, H, D) against a (B, H, Skv, D) cache.
+
+    Returns ``out`` (B, H, D).  See include/attn.h.
+    """
+    _check_tensor("q", q, 3)
+    _check_tensor("kcache", kcache, 4)
+    _check_tensor("vcache", vcache, 4)
+    B, H, D = q.shape
+    Skv = kcache.shape[2]
+    if tuple(kcache.shape) != (B, H, Skv, D) or tuple(vcache.shape) != (B, H, Skv, D):
+        raise ValueError("kcache and vcache must be (B, H, Skv, D) matching q")
+    if not (q.dtype == kcache.dtype == vcache.dtype):
+        raise TypeError("q, kcache, vcache must share one dtype")
+    if out is None:
+        out = _torch().empty_like(q)
+    _check_tensor("out", out, 3)
+    kl = _kv_len_arg(kv_len, B, q.device)
+    rc = lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, Skv, D, _ptr(kl),
+                           _dtype_code(q), _stream_handle(stream))
+    _check(rc)
+    return out
+
+
+def attn_decode_splits(B: int, H: int, Skv: int, D: int) -> int:
+    return lib().attn_decode_splits(B, H, Skv, D)
+
+
+def attn_device_status(stream=None) -> None:
+    """Synchronise the stream and raise AttnError if a kernel reported a timeout."""
+    _check(lib().attn_device_status(_stream_handle(stream)))
+
+
+def attn_release() -> None:
+    lib().attn_release()
+
+
+__all__ = [
+    "attn_fwd", "attn_decode", "attn_decode_splits", "attn_device_status", "attn_release",
+    "attn_last_error", "lib", "AttnError", "SIGNATURES", "LIB_PATH",
+    "ATTN_F32", "ATTN_BF16", "ATTN_OK", "ATTN_EINVAL", "ATTN_EUNSUPPORTED", "ATTN_ECUDA",
+    "ATTN_ENOMEM", "ATTN_ETIMEOUT",
+]

@@ -1,0 +1,325 @@
+// C-ABI shim: argument validation, kernel dispatch, TMA descriptor encoding,
+// decode workspace and the device status word.  The contract of every entry
+// point is documented in include/attn.h.
+#include "attn.h"
+#include "kernels.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <mutex>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+namespace attn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(ATTN_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte ranges [a, a + na) and [b, b + nb) overlap?
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// ------------------------------------------------------------ device status word
+
+__device__ int g_status_word;
+
+std::mutex g_mutex;
+int *g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+int current_device(int *dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (*dev < 0 || *dev >= kMaxDevices) return fail(ATTN_EUNSUPPORTED, "device ordinal %d out of range", *dev);
+    return ATTN_OK;
+}
+
+int status_word(int **out) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_status_ptr[dev];
+    return ATTN_OK;
+}
+
+int num_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_num_sms[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_num_sms[dev] = n;
+    }
+    return g_num_sms[dev];
+}
+
+// ------------------------------------------------------------ TMA descriptors
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+
+int get_encode(EncodeTiledFn *fn) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !p)
+            return fail(ATTN_ECUDA, "cuTensorMapEncodeTiled entry point unavailable");
+        g_encode = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    *fn = g_encode;
+    return ATTN_OK;
+}
+
+// (D, S, B*H) bf16 view of a (B, H, S, D) tensor; boxes of 64 x 128 x 1 with
+// 128-byte swizzle, out-of-range rows read as zero.
+int make_map(CUtensorMap *map, const void *base, int D, int S, long long BH) {
+    EncodeTiledFn encode;
+    int rc = get_encode(&encode);
+    if (rc) return rc;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                   static_cast<cuuint64_t>(S) * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
+// ------------------------------------------------------------ decode workspace
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+
+int workspace(size_t bytes, void **out) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Workspace &w = g_ws[dev];
+    if (w.bytes < bytes) {
+        if (w.ptr) cudaFree(w.ptr);  // synchronises the device: no call still uses it
+        w.ptr = nullptr;
+        w.bytes = 0;
+        cudaError_t e = cudaMalloc(&w.ptr, bytes);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            return fail(ATTN_ENOMEM, "decode workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
+        }
+        w.bytes = bytes;
+    }
+    *out = w.ptr;
+    return ATTN_OK;
+}
+
+int decode_chunk(int B, int H, int Skv) {
+    // Aim for at least ~6 CTAs per SM; shorter chunks only when the batch is small.
+    const long long want = 6LL * num_sms();
+    int chunk = 512;
+    while (chunk > 64 && static_cast<long long>(B) * H * ((Skv + chunk - 1) / chunk) < want) chunk /= 2;
+    return chunk;
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+ATTN_API const char *attn_last_error(void) { return g_last_error; }
+
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int Sq,
+                      int Skv, int D, float scale, int causal, const int32_t *kv_len, int dtype,
+                      void *stream) {
+    g_last_error[0] = '\0';
+    if (B < 1 || H < 1 || Sq < 0 || Skv < 0)
+        return fail(ATTN_EINVAL, "attn_fwd: need B >= 1, H >= 1, Sq >= 0, Skv >= 0 (got %d, %d, %d, %d)", B, H, Sq, Skv);
+    if ((Sq > 0 && (!q || !out)) || (Skv > 0 && (!k || !v)))
+        return fail(ATTN_EINVAL, "attn_fwd: q and out (Sq > 0), k and v (Skv > 0) must not be NULL");
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return fail(ATTN_EINVAL, "attn_fwd: unknown dtype %d", dtype);
+    if (D <= 0) return fail(ATTN_EINVAL, "attn_fwd: D must be positive (got %d)", D);
+    if (D != 64 && D != 128) return fail(ATTN_EUNSUPPORTED, "attn_fwd: D = %d not supported (64 or 128)", D);
+    if (!(scale >= 0.f) || isinf(scale)) return fail(ATTN_EINVAL, "attn_fwd: scale must be finite and >= 0");
+    if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_fwd: causal must be 0 or 1");
+    if (causal && Sq > Skv) return fail(ATTN_EINVAL, "attn_fwd: causal needs Sq <= Skv (got %d > %d)", Sq, Skv);
+    if (kv_len && Sq != Skv) return fail(ATTN_EINVAL, "attn_fwd: kv_len needs Sq == Skv (self-attention)");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+        return fail(ATTN_EINVAL, "attn_fwd: q, k, v and out must be 16-byte aligned");
+    if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
+        return fail(ATTN_EINVAL, "attn_fwd: kv_len must be 4-byte aligned");
+    const long long bh = static_cast<long long>(B) * H;
+    const long long rows = bh * (Sq > Skv ? Sq : Skv);
+    if (rows >= (1LL << 31) || bh > 65535LL * 65535LL)
+        return fail(ATTN_EINVAL, "attn_fwd: B*H*S = %lld rows is too large", rows);
+    const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
+    const size_t q_bytes = static_cast<size_t>(bh) * Sq * D * esz;
+    const size_t kv_bytes = static_cast<size_t>(bh) * Skv * D * esz;
+    if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||
+        overlaps(out, q_bytes, v, kv_bytes))
+        return fail(ATTN_EINVAL, "attn_fwd: out overlaps an input");
+    if (Sq == 0) return ATTN_OK;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Skv == 0) {  // no row sees a key
+        cudaError_t e = launch_zero_fill(out, q_bytes, st);
+        return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd zero fill");
+    }
+    int *status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    FwdArgs a{q, k, v, out, kv_len, B, H, Sq, Skv, D, scale, causal, status, st};
+    cudaError_t e;
+    if (dtype == ATTN_F32) {
+        if (B > 65535 || H > 65535) return fail(ATTN_EINVAL, "attn_fwd: B and H must be <= 65535 for fp32");
+        e = launch_prefill_f32(a);
+    } else {
+        CUtensorMap tq, tk, tv;
+        if ((rc = make_map(&tq, q, D, Sq, bh)) || (rc = make_map(&tk, k, D, Skv, bh)) ||
+            (rc = make_map(&tv, v, D, Skv, bh)))
+            return rc;
+        e = launch_prefill_tc(a, tq, tk, tv);
+    }
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd launch");
+}
+
+ATTN_API int attn_decode_splits(int B, int H, int Skv, int D) {
+    if (B < 1 || H < 1 || Skv < 0 || (D != 64 && D != 128)) return ATTN_EINVAL;
+    const int chunk = decode_chunk(B, H, Skv);
+    const int n = (Skv + chunk - 1) / chunk;
+    return n > 0 ? n : 1;
+}
+
+ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, void *out, int B,
+                         int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream) {
+    g_last_error[0] = '\0';
+    if (B < 1 || H < 1 || Skv < 0)
+        return fail(ATTN_EINVAL, "attn_decode: need B >= 1, H >= 1, Skv >= 0 (got %d, %d, %d)", B, H, Skv);
+    if (!q || !out || (Skv > 0 && (!kcache || !vcache)))
+        return fail(ATTN_EINVAL, "attn_decode: q, out and (for Skv > 0) kcache, vcache must not be NULL");
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return fail(ATTN_EINVAL, "attn_decode: unknown dtype %d", dtype);
+    if (D <= 0) return fail(ATTN_EINVAL, "attn_decode: D must be positive (got %d)", D);
+    if (dtype != ATTN_BF16) return fail(ATTN_EUNSUPPORTED, "attn_decode: only bf16 is implemented");
+    if (D != 64 && D != 128) return fail(ATTN_EUNSUPPORTED, "attn_decode: D = %d not supported (64 or 128)", D);
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return fail(ATTN_EINVAL, "attn_decode: q, kcache, vcache and out must be 16-byte aligned");
+    if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
+        return fail(ATTN_EINVAL, "attn_decode: kv_len must be 4-byte aligned");
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh * (Skv > 1 ? Skv : 1) >= (1LL << 31) || bh >= (1LL << 31) / 64)
+        return fail(ATTN_EINVAL, "attn_decode: B*H*Skv is too large");
+    const size_t qo_bytes = static_cast<size_t>(bh) * D * 2;
+    const size_t kv_bytes = static_cast<size_t>(bh) * Skv * D * 2;
+    if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, kcache, kv_bytes) ||
+        overlaps(out, qo_bytes, vcache, kv_bytes))
+        return fail(ATTN_EINVAL, "attn_decode: out overlaps an input");
+
+    const int chunk = decode_chunk(B, H, Skv);
+    const int n_split = attn_decode_splits(B, H, Skv, D);
+    const size_t o_bytes = static_cast<size_t>(bh) * n_split * D * sizeof(float);
+    const size_t ml_bytes = static_cast<size_t>(bh) * n_split * 2 * sizeof(float);
+    void *ws = nullptr;
+    int rc = workspace(o_bytes + ml_bytes, &ws);
+    if (rc) return rc;
+    int *status = nullptr;
+    if ((rc = status_word(&status))) return rc;
+    DecodeArgs a{q, kcache, vcache, out, kv_len, B, H, Skv, D, 1.0f / sqrtf(static_cast<float>(D)),
+                 chunk, n_split, static_cast<float *>(ws),
+                 reinterpret_cast<float *>(static_cast<char *>(ws) + o_bytes), status,
+                 static_cast<cudaStream_t>(stream)};
+    cudaError_t e = launch_decode(a);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode launch");
+}
+
+ATTN_API int attn_device_status(void *stream) {
+    g_last_error[0] = '\0';
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_device_status: stream synchronize");
+    int *status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    int word = 0;
+    e = cudaMemcpy(&word, status, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_device_status: read status word");
+    if (word == 0) return ATTN_OK;
+    const int zero = 0;
+    e = cudaMemcpy(status, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_device_status: clear status word");
+    return fail(ATTN_ETIMEOUT, "a device-side wait gave up (site 0x%x); that call's output is undefined",
+                word >> 8);
+}
+
+ATTN_API void attn_release(void) {
+    int dev;
+    if (current_device(&dev)) return;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_ws[dev].ptr) cudaFree(g_ws[dev].ptr);
+    g_ws[dev].ptr = nullptr;
+    g_ws[dev].bytes = 0;
+}
+
+}  // extern "C"
+
+namespace attn {
+
+namespace {
+__global__ void zero_fill_kernel(uint4 *out, size_t n) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        out[i] = make_uint4(0, 0, 0, 0);
+}
+}  // namespace
+
+cudaError_t launch_zero_fill(void *out, size_t n_bytes, cudaStream_t stream) {
+    const size_t n = n_bytes / 16;
+    if (n == 0) return cudaSuccess;
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    zero_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(static_cast<uint4 *>(out), n);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,54 @@
+// Internal interface between the C-ABI shim (api.cu) and the kernel files.
+// Arguments arrive here already validated by the shim.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct FwdArgs {
+    const void *q, *k, *v;  // (B, H, Sq|Skv, D), device
+    void *out;              // (B, H, Sq, D), device
+    const int32_t *kv_len;  // device int32[B] or nullptr
+    int B, H, Sq, Skv, D;
+    float scale;            // multiplier of Q K^T
+    int causal;
+    int *status;            // device status word
+    cudaStream_t stream;
+};
+
+struct DecodeArgs {
+    const void *q;          // (B, H, D) bf16
+    const void *k, *v;      // (B, H, Skv, D) bf16
+    void *out;              // (B, H, D) bf16
+    const int32_t *kv_len;  // device int32[B] or nullptr
+    int B, H, Skv, D;
+    float scale;
+    int chunk;              // keys per split (multiple of 64, <= kDecodeMaxChunk)
+    int n_split;            // ceil(Skv / chunk), >= 1
+    float *part_o;          // B*H*n_split*D fp32 partial outputs
+    float *part_ml;         // B*H*n_split*2 fp32 (running max in log2 units, sum)
+    int *status;
+    cudaStream_t stream;
+};
+
+constexpr int kDecodeMaxChunk = 1024;
+
+// fp32 SIMT prefill (D in {64, 128}).
+cudaError_t launch_prefill_f32(const FwdArgs &a);
+
+// bf16 tcgen05 prefill (D in {64, 128}); tq/tk/tv are 3-D tensor maps over
+// (D, S, B*H) with 64 x 128 x 1 boxes and 128-byte swizzle.
+cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                              const CUtensorMap &tv);
+
+// bf16 split-KV decode: partial kernel then combine kernel.
+cudaError_t launch_decode(const DecodeArgs &a);
+
+// Writes zeros over n bytes (multiple of 16, 16-byte aligned) -- degenerate
+// calls whose every row sees no key.
+cudaError_t launch_zero_fill(void *out, size_t n_bytes, cudaStream_t stream);
+
+}  // namespace attn
