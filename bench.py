@@ -108,7 +108,8 @@ class ClockSampler:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,timestamp")
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -116,14 +117,24 @@ class ClockSampler:
         self.file = None
 
     def start(self):
+        """Start sampling and wait (up to 5 s) until the first sample is written."""
+        self.window = None
         try:
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and os.path.getsize(self.file.name) == 0:
+            time.sleep(0.01)
+
+    def mark(self, t_begin, t_end):
+        """Wall-clock bounds (time.time()) of the timed region."""
+        self.window = (t_begin, t_end)
 
     def stop(self):
         if self.proc is None:
@@ -139,6 +150,20 @@ class ClockSampler:
         os.unlink(self.file.name)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        inside = []
+        for r in rows:
+            r = [x.strip() for x in r]
+            if len(r) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[9].split(".")[0], "%Y/%m/%d %H:%M:%S")) + \
+                    float("0." + r[9].split(".")[1]) if "." in r[9] else 0.0
+            except (ValueError, IndexError):
+                ts = 0.0
+            if self.window and self.window[0] - 0.05 <= ts <= self.window[1] + 0.05:
+                inside.append(r)
+        if inside:
+            rows = inside
         for r in rows:
             r = [x.strip() for x in r]
             if len(r) < 9:
@@ -154,7 +179,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "samples_in_timed_region": len(inside), "period_ms": self.PERIOD_MS}
 
 
 # ----------------------------------------------------------------------------- timing
@@ -173,15 +199,16 @@ def time_steps(fn, steps, stream, flush):
     return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
-def kernel_source_digest():
+def kernel_source_digest(main="prefill_tc.cu"):
+    """Short hash of a kernel's source files (the kernel file, ptx.cuh, kernels.h)."""
     h = hashlib.sha256()
-    for f in ("prefill_tc.cu", "ptx.cuh", "kernels.h"):
+    for f in (main, "ptx.cuh", "kernels.h"):
         with open(os.path.join(ROOT, "transformer_scaled_dot_fwd_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name):
+def profiled_traffic(name, main):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source; otherwise None."""
     path = os.path.join(ROOT, "profiles", name)
@@ -191,7 +218,7 @@ def profiled_traffic(name):
         return None
     m_src = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
     m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_src and m_b) or m_src.group(1) != kernel_source_digest():
+    if not (m_src and m_b) or m_src.group(1) != kernel_source_digest(main):
         return None
     return float(m_b.group(1))
 
@@ -312,10 +339,11 @@ def run_ours(args):
     barrier(dist, device)
     torch.cuda.synchronize()
     sampler.start()
-    wall0 = time.perf_counter()
+    wall0, tw0 = time.perf_counter(), time.time()
     ms = time_steps(step, args.steps, stream, flush)
     torch.cuda.synchronize()
-    wall = time.perf_counter() - wall0
+    wall, tw1 = time.perf_counter() - wall0, time.time()
+    sampler.mark(tw0, tw1)
     clocks = sampler.stop()
     barrier(dist, device)
     attn.attn_device_status()
@@ -325,7 +353,7 @@ def run_ours(args):
     avg_ms = float(sum(ms)) / args.steps
     achieved = flops_step / (avg_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    traffic = profiled_traffic("prefill_tc_B4H32S2048D128.md")
+    traffic = profiled_traffic("prefill_tc_B4H32S2048D128.md", "prefill_tc.cu")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16 dense (burst: the kernel is timed alone)",
@@ -386,7 +414,9 @@ def decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, 
         "splits_per_head": attn.attn_decode_splits(dwk.B, dwk.H, dwk.Skv, dwk.D),
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": d_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": d_gbs / hbm_peak, "traffic": None,
+                     "frac": d_gbs / hbm_peak,
+                     "traffic": profiled_traffic("decode_partial_B64H32Skv8192D128.md", "decode.cu")
+                     if not args.decode_batch else None,
                      "peak_source": f"{peak_src} HBM copy bandwidth",
                      "algorithmic_bytes_per_launch": dbytes},
     }
@@ -437,7 +467,7 @@ def e2e_leg(args, attn, q, k, v, out, w, flops_step, world, dist, device):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,

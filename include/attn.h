@@ -136,6 +136,18 @@ ATTN_API int attn_decode_splits(int B, int H, int Skv, int D);
  */
 ATTN_API int attn_device_status(void *stream);
 
+/*
+ * attn_selftest_wait_timeout -- diagnostic: enqueue a one-warp kernel whose
+ * only device-side wait can never complete, with a limit of `limit_cycles` SM
+ * clock cycles (0 .. 2e9).  The wait gives up, the kernel records the timeout
+ * in the device status word and exits, so the next attn_device_status(stream)
+ * returns ATTN_ETIMEOUT (and clears the word).  Used to check, on a real
+ * device and without any fault or hang, the path every kernel's bounded waits
+ * take when a logic error would otherwise deadlock.  There is no counterpart
+ * on the pages.
+ */
+ATTN_API int attn_selftest_wait_timeout(long long limit_cycles, void *stream);
+
 /* Description of the last error on the calling thread ("" if none). */
 ATTN_API const char *attn_last_error(void);
 

@@ -25,7 +25,7 @@
  *   - "Scaled dot-product attention with masking", "The math" and "Adding the
  *     causal mask" (decode: a single query sees every cached key).
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings where the pages leave a step open:
  *   1. Forbidden keys are EXCLUDED from the max, the sum and the mixture.
  *      This is the exact value of adding -inf before the softmax, written
  *      without inf arithmetic.

@@ -93,3 +93,16 @@ def test_repeat_calls_are_deterministic(gpu):
     again = attn.attn_decode(q, kc, vc, kv_len=kl)
     attn.attn_device_status()
     assert torch.equal(out, again)
+
+
+def test_device_wait_timeout_is_reported(gpu):
+    """A device-side wait that can never complete gives up after its limit and
+    surfaces as ATTN_ETIMEOUT on the host; the context stays usable."""
+    attn.attn_device_status()  # clean slate
+    attn.attn_selftest_wait_timeout(1_000_000)
+    with pytest.raises(attn.AttnError) as e:
+        attn.attn_device_status()
+    assert e.value.code == attn.ATTN_ETIMEOUT
+    attn.attn_device_status()  # the word was cleared
+    _, _, _, out, ref = decode_case(1, 2, 300, 128, seed=77)  # and the device still works
+    assert_close(out, ref, torch.bfloat16, "after timeout self-test")

@@ -37,6 +37,7 @@ SIGNATURES = {
     "attn_device_status": (_i, [_vp]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_release": (None, []),
+    "attn_selftest_wait_timeout": (_i, [ctypes.c_longlong, _vp]),
 }
 
 _lib = None
@@ -187,13 +188,18 @@ def attn_device_status(stream=None) -> None:
     _check(lib().attn_device_status(_stream_handle(stream)))
 
 
+def attn_selftest_wait_timeout(limit_cycles: int = 1_000_000, stream=None) -> None:
+    """Enqueue the diagnostic kernel whose wait runs out (see include/attn.h)."""
+    _check(lib().attn_selftest_wait_timeout(int(limit_cycles), _stream_handle(stream)))
+
+
 def attn_release() -> None:
     lib().attn_release()
 
 
 __all__ = [
     "attn_fwd", "attn_decode", "attn_decode_splits", "attn_device_status", "attn_release",
-    "attn_last_error", "lib", "AttnError", "SIGNATURES", "LIB_PATH",
+    "attn_last_error", "attn_selftest_wait_timeout", "lib", "AttnError", "SIGNATURES", "LIB_PATH",
     "ATTN_F32", "ATTN_BF16", "ATTN_OK", "ATTN_EINVAL", "ATTN_EUNSUPPORTED", "ATTN_ECUDA",
     "ATTN_ENOMEM", "ATTN_ETIMEOUT",
 ]

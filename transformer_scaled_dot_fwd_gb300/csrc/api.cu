@@ -3,6 +3,7 @@
 // point is documented in include/attn.h.
 #include "attn.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -292,6 +293,17 @@ ATTN_API int attn_device_status(void *stream) {
                 word >> 8);
 }
 
+ATTN_API int attn_selftest_wait_timeout(long long limit_cycles, void *stream) {
+    g_last_error[0] = '\0';
+    if (limit_cycles < 0 || limit_cycles > kWaitLimitCycles)
+        return fail(ATTN_EINVAL, "attn_selftest_wait_timeout: limit must be in [0, %lld] cycles", kWaitLimitCycles);
+    int *status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    cudaError_t e = launch_wait_timeout_probe(limit_cycles, status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_selftest_wait_timeout launch");
+}
+
 ATTN_API void attn_release(void) {
     int dev;
     if (current_device(&dev)) return;
@@ -306,12 +318,33 @@ ATTN_API void attn_release(void) {
 namespace attn {
 
 namespace {
+// Waits on an mbarrier phase that nothing completes, with a short limit, so
+// that the timeout path (abort flag, status word) runs without a hang.
+__global__ void wait_timeout_probe_kernel(long long limit, int *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag, limit)) report_timeout(status, 0x7f);
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_arrive(&bar);  // complete the phase before the CTA exits
+}
+
 __global__ void zero_fill_kernel(uint4 *out, size_t n) {
     for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<size_t>(gridDim.x) * blockDim.x)
         out[i] = make_uint4(0, 0, 0, 0);
 }
 }  // namespace
+
+cudaError_t launch_wait_timeout_probe(long long limit, int *status, cudaStream_t stream) {
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(limit, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_zero_fill(void *out, size_t n_bytes, cudaStream_t stream) {
     const size_t n = n_bytes / 16;

@@ -47,6 +47,10 @@ cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUt
 // bf16 split-KV decode: partial kernel then combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a);
 
+// One-warp kernel whose only wait can never complete: exercises the bounded
+// wait and the status word (attn_selftest_wait_timeout).
+cudaError_t launch_wait_timeout_probe(long long limit, int *status, cudaStream_t stream);
+
 // Writes zeros over n bytes (multiple of 16, 16-byte aligned) -- degenerate
 // calls whose every row sees no key.
 cudaError_t launch_zero_fill(void *out, size_t n_bytes, cudaStream_t stream);

@@ -8,7 +8,8 @@
 // masking", "The memory problem"), redesigned here for Blackwell.
 //
 // One CTA owns two 128-row query tiles (Q0, Q1) of one (b, h) and streams the
-// 128-key K/V tiles they need through shared memory.  Roles:
+// 128-key K/V tiles they need through shared memory.  Roles (12 warps; the
+// first warpgroup gives registers to the two softmax warpgroups):
 //   warp 0      TMA producer: Q0/Q1 once, then K_j, V_j into a ring of
 //               32 KB stages (128-byte swizzle, 64-column boxes).
 //   warp 1      allocates 512 TMEM columns; lane 0 issues every MMA:
@@ -16,7 +17,7 @@
 //                 O_x += P_x V_j         (TS: P read from TMEM, V MN-major)
 //               in the order S0_0 S1_0 | PV0_j S0_{j+1} PV1_j S1_{j+1} | ...
 //               so each softmax warpgroup has two MMA slots to hide behind.
-//   warps 2-5   softmax for Q0, warps 6-9 for Q1: thread = query row = TMEM
+//   warps 4-7   softmax for Q0, warps 8-11 for Q1: thread = query row = TMEM
 //               lane.  Load the 128 fp32 scores of the row, mask (only on
 //               tiles that cross the causal diagonal or the padding edge),
 //               online max/sum in log2 units, p = 2^(s*scale*log2e - m),
@@ -37,10 +38,18 @@ namespace {
 constexpr int kBM = 128;       // query rows per Q tile (one TMEM lane each)
 constexpr int kBN = 128;       // keys per K/V tile
 constexpr int kQTiles = 2;     // Q tiles per CTA
-constexpr int kThreads = 320;  // 10 warps
+constexpr int kThreads = 384;  // 12 warps
+constexpr uint32_t kRegsProducer = 64;   // warps 0-3 after setmaxnreg
+constexpr uint32_t kRegsSoftmax = 216;   // warps 4-11: 128*64 + 256*216 <= 384*168
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
+#ifdef ATTN_TRACE
+constexpr int kTraceRoles = 4, kTraceEvents = 512;
+constexpr int kTraceBytes = kTraceRoles * kTraceEvents * 8;  // timeline probes (profiling builds)
+#else
+constexpr int kTraceBytes = 0;
+#endif
 
 template <int D>
 struct Layout {
@@ -50,13 +59,14 @@ struct Layout {
     static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring depth
     static constexpr int kRingOff = kQTiles * kTileBytes;
     static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
+    static constexpr int kSmemBytes = kBarOff + 512 + kTraceBytes + 1024;  // + barriers (+ probes) + slack
     // TMEM column of S_x (and of P_x, which aliases it) and of O_x
     static __device__ __forceinline__ uint32_t s_col(int x) { return static_cast<uint32_t>(x) * 128u; }
     static __device__ __forceinline__ uint32_t o_col(int x) { return 256u + static_cast<uint32_t>(x) * D; }
 };
 
 struct Bars {
+    long long t0;  // CTA start clock (timeline probes)
     uint64_t q_full;
     uint64_t kv_full[8];
     uint64_t kv_empty[8];
@@ -67,6 +77,40 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
 };
+
+// Timeline probes for profiling builds (compiled out unless ATTN_TRACE is
+// defined): in chosen CTAs, the TMA thread, the MMA thread and one thread of
+// each softmax warpgroup record (event, SM clock since CTA start) in shared
+// memory; the CTA copies its record to global memory when it finishes.
+#ifdef ATTN_TRACE
+__device__ long long *g_trace_buf;
+__device__ int g_trace_ctas[4];
+extern "C" __attribute__((visibility("default"))) int attn_trace_set(long long *buf, const int *ctas) {
+    cudaMemcpyToSymbol(g_trace_buf, &buf, sizeof buf);
+    return static_cast<int>(cudaMemcpyToSymbol(g_trace_ctas, ctas, 4 * sizeof(int)));
+}
+#define TRACE_SETUP(t0_smem)                                                        \
+    int trace_slot = -1, trace_n = 0;                                               \
+    for (int ts = 0; ts < 4; ++ts)                                                  \
+        if (g_trace_ctas[ts] == static_cast<int>(blockIdx.x) && g_trace_buf) trace_slot = ts; \
+    long long *trace_smem = reinterpret_cast<long long *>(smem + L::kBarOff + 512);           \
+    if (threadIdx.x == 0) t0_smem = clock64();
+#define TRACE(role, code, t0)                                                       \
+    do {                                                                            \
+        if (trace_slot >= 0 && trace_n < kTraceEvents)                              \
+            trace_smem[(role) * kTraceEvents + trace_n++] =                         \
+                (static_cast<long long>(code) << 40) | (clock64() - (t0));          \
+    } while (0)
+#define TRACE_FLUSH()                                                               \
+    if (trace_slot >= 0) {                                                          \
+        for (int ti = threadIdx.x; ti < kTraceRoles * kTraceEvents; ti += blockDim.x) \
+            g_trace_buf[trace_slot * kTraceRoles * kTraceEvents + ti] = trace_smem[ti]; \
+    }
+#else
+#define TRACE_SETUP(t0_smem)
+#define TRACE(role, code, t0)
+#define TRACE_FLUSH()
+#endif
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
@@ -84,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars &bars = *reinterpret_cast<Bars *>(smem + L::kBarOff);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    TRACE_SETUP(bars.t0)
 
     // ---- work unit: longest query-tile pairs first (causal cost grows with the row)
     const int BH = a.B * a.H;
@@ -133,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ================================================================ TMA producer
+        regs_dec<kRegsProducer>();
         if (lane == 0 && N > 0) {
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
@@ -158,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    TRACE(0, 300 + kv + j * 1000, bars.t0);
                     mbar_arrive_expect_tx(&bars.kv_full[slot], L::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < L::kSub; ++c)
@@ -174,27 +221,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
+        regs_dec<kRegsProducer>();
         if (lane == 0 && N > 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
             const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 1);
-            const uint32_t q_addr = smem_u32(smem), ring_addr = smem_u32(ring);
+            // Base descriptors, built once: the K-step offsets only move the
+            // start-address field (low 14 bits, no carry below 256 KB).
+            const uint64_t dq[2] = {sdesc_sw128(smem_u32(smem), 16, 1024),
+                                    sdesc_sw128(smem_u32(smem) + L::kTileBytes, 16, 1024)};
+            const uint64_t dk0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(ring), L::kBlockBytes, 1024);
             auto issue_s = [&](int x, int slot) {
-                const uint32_t qa = q_addr + x * L::kTileBytes;
-                const uint32_t ka = ring_addr + slot * L::kTileBytes;
+                const uint64_t da = dq[x];
+                const uint64_t db = desc_add(dk0, (slot * L::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk / 4) * L::kBlockBytes + (kk % 4) * 32;
-                    mma_ss(tmem + L::s_col(x), sdesc_sw128(qa + koff, 16, 1024),
-                           sdesc_sw128(ka + koff, 16, 1024), idesc_s, kk > 0);
+                    const uint32_t koff = ((kk / 4) * L::kBlockBytes + (kk % 4) * 32) >> 4;
+                    mma_ss(tmem + L::s_col(x), desc_add(da, koff), desc_add(db, koff), idesc_s, kk > 0);
                 }
             };
             auto issue_pv = [&](int x, int slot, bool acc) {
-                const uint32_t va = ring_addr + slot * L::kTileBytes;
+                const uint64_t db = desc_add(dv0, (slot * L::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + L::o_col(x), tmem + L::s_col(x) + kk * 8,
-                           sdesc_sw128(va + kk * 16 * 128, L::kBlockBytes, 1024), idesc_o,
-                           (acc || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + L::o_col(x), tmem + L::s_col(x) + kk * 8, desc_add(db, (kk * 16 * 128) >> 4),
+                           idesc_o, (acc || kk > 0) ? 1u : 0u);
             };
             int consumed = 0;
             uint32_t pr[2] = {0, 0};
@@ -215,12 +266,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             for (int j = 0; j < N && ok; ++j) {
+                TRACE(1, 100 + j * 1000, bars.t0);
                 const int vslot = consumed % L::kStages;
                 if (!(ok = mbar_wait(&bars.kv_full[vslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                 ++consumed;
                 tc_fence_after();
+                TRACE(1, 101 + j * 1000, bars.t0);
                 if (j < n_kv[0]) {
                     if (!(ok = mbar_wait(&bars.p_ready[0], pr[0], &bars.abort))) break;
+                    TRACE(1, 102 + j * 1000, bars.t0);
                     pr[0] ^= 1;
                     tc_fence_after();
                     issue_pv(0, vslot, j > 0);
@@ -238,8 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_commit(&bars.s_full[0]);
                     }
                 }
+                TRACE(1, 103 + j * 1000, bars.t0);
                 if (j < n_kv[1]) {
                     if (!(ok = mbar_wait(&bars.p_ready[1], pr[1], &bars.abort))) break;
+                    TRACE(1, 104 + j * 1000, bars.t0);
                     pr[1] ^= 1;
                     tc_fence_after();
                     issue_pv(1, vslot, j > 0);
@@ -259,9 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int never = 0;
             mbar_wait(&bars.mma_done, 0, &never);
         }
+    } else if (warp < 4) {
+        regs_dec<kRegsProducer>();  // warps 2-3: no role, registers go to the softmax warps
     } else {
         // ================================================================ softmax + epilogue
-        const int x = (warp - 2) / 4;
+        regs_inc<kRegsSoftmax>();
+        const int x = (warp - 4) / 4;
         const int quarter = warp % 4;  // TMEM lanes [32*quarter, 32*quarter + 32)
         const int r = quarter * 32 + lane;
         const int i = (pair * kQTiles + x) * kBM + r;  // query row
@@ -275,8 +334,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sp = 0;
         bool ok = true;
 
+        const bool tr = lane == 0 && (quarter == 0);
         for (int j = 0; j < n; ++j) {
+            if (tr) TRACE(2 + x, 200 + x * 10 + j * 1000, bars.t0);
             if (!(ok = mbar_wait_warp(&bars.s_full[x], sp, &bars.abort))) break;
+            if (tr) TRACE(2 + x, 201 + x * 10 + j * 1000, bars.t0);
             sp ^= 1;
             tc_fence_after();
             uint32_t s[128];
@@ -286,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) reg_fence32(s + c * 32);
 
+            if (tr) TRACE(2 + x, 202 + x * 10 + j * 1000, bars.t0);
             const int kbase = j * kBN;
             const bool need_mask = __any_sync(0xffffffffu, kbase + kBN > lim);
             if (need_mask) {
@@ -293,13 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 128; ++c)
                     if (kbase + c >= lim) s[c] = f2u(-INFINITY);
             }
+            // row max over the tile: 8 chains of 3-input max
             float m8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = u2f(s[e]);
+            for (int e = 0; e < 8; ++e) m8[e] = fmaxf(u2f(s[2 * e]), u2f(s[2 * e + 1]));
 #pragma unroll
-            for (int c = 8; c < 128; ++c) m8[c % 8] = fmaxf(m8[c % 8], u2f(s[c]));
-            const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int c = 16; c < 128; c += 2)
+                m8[(c / 2) % 8] = fmax3(m8[(c / 2) % 8], u2f(s[c]), u2f(s[c + 1]));
+            const float mraw = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
             const float m_tile = mraw == -INFINITY ? -INFINITY : mraw * sl2;
             const float m_new = fmaxf(m_run, m_tile);
             const bool grow = m_new > m_run + kRescaleLog2;
@@ -322,33 +386,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (tr) TRACE(2 + x, 203 + x * 10 + j * 1000, bars.t0);
             const float negm = m_run == -INFINITY ? 0.f : -m_run;
-            float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(negm, negm);
+            uint64_t l4[4] = {0, 0, 0, 0};  // packed partial row sums
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // two halves of 64 keys -> 32 packed columns each
                 uint32_t p[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) {
-                    const float s0 = u2f(s[h * 64 + 2 * e]), s1 = u2f(s[h * 64 + 2 * e + 1]);
-                    float p0 = ex2_approx(fmaf(s0, sl2, negm));
-                    float p1 = ex2_approx(fmaf(s1, sl2, negm));
+                    const uint64_t arg = ffma2(f2_pack(u2f(s[h * 64 + 2 * e]), u2f(s[h * 64 + 2 * e + 1])),
+                                               sl2x2, negmx2);
+                    float p0 = ex2_approx(f2_lo(arg));
+                    float p1 = ex2_approx(f2_hi(arg));
                     if (need_mask) {  // exact zeros, also when scale == 0
-                        p0 = s0 == -INFINITY ? 0.f : p0;
-                        p1 = s1 == -INFINITY ? 0.f : p1;
+                        p0 = u2f(s[h * 64 + 2 * e]) == -INFINITY ? 0.f : p0;
+                        p1 = u2f(s[h * 64 + 2 * e + 1]) == -INFINITY ? 0.f : p1;
                     }
-                    l8[(2 * e) % 8] += p0;
-                    l8[(2 * e + 1) % 8] += p1;
+                    l4[e % 4] = fadd2(l4[e % 4], f2_pack(p0, p1));
                     p[e] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(t_s + h * 32, p);
             }
-            l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+            {
+                const uint64_t l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
+                l += f2_lo(l2) + f2_hi(l2);
+            }
+            if (tr) TRACE(2 + x, 204 + x * 10 + j * 1000, bars.t0);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars.p_ready[x]);
+            if (tr) TRACE(2 + x, 205 + x * 10 + j * 1000, bars.t0);
         }
 
         // ---- epilogue
+        if (tr) TRACE(2 + x, 290 + x, bars.t0);
         bool have_o = n > 0 && ok;
         if (have_o) {
             have_o = mbar_wait_warp(&bars.o_full[x], 0, &bars.abort);
@@ -382,8 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (lane == 0 && warp >= 4 && warp % 4 == 0) TRACE(2 + (warp - 4) / 4, 299, bars.t0);
     tc_fence_before();
     __syncthreads();
+    TRACE_FLUSH();
     if (warp == 1) {
         tc_fence_after();
         __syncwarp();
