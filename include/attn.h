@@ -123,6 +123,37 @@ ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, 
                          int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode that never allocates device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * must not allocate device memory while they run.  attn_decode allocates its
+ * scratch (the per-chunk partial results) with cudaMalloc on first use and
+ * whenever a call needs more; that fails or misbehaves for callers that have
+ * reserved all device memory up front for their own pool (an inference server
+ * sizing its KV cache to the whole GPU), and cudaMalloc / cudaFree can
+ * synchronise the device, which a latency-bound decode loop cannot afford.
+ * This variant runs the same kernels with the scratch in a fixed array inside
+ * the library instead, so it calls no allocation routine at all.
+ *
+ * Arguments, layouts, dtype support and results are those of attn_decode.
+ * Limit: B*H*attn_decode_splits(B,H,Skv,D)*(D + 2)*4 bytes must not exceed
+ * 32 MiB (33554432); larger requests return ATTN_EINVAL with a message saying
+ * how much they need (B64 H32 Skv8192 D128 needs about 17 MB).
+ *
+ * The array is part of the library image: every GPU that loads the library's
+ * decode code holds these 32 MiB until the process exits.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current) and caches it; make that first call before any stream
+ * capture on the device.  All calls on a device share the one array and its
+ * contents persist between calls (nothing in it needs to start at zero: each
+ * call writes every partial it reads), so calls that overlap on the GPU (on
+ * different streams, or from different threads) race and must be serialised
+ * by the caller.
+ */
+ATTN_API int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, void *out, int B,
+                                 int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream);
+
+/*
  * attn_decode_splits -- number of KV chunks attn_decode uses per (batch,
  * head) for these sizes (for benchmarks and tests); negative on bad sizes.
  */

@@ -33,6 +33,7 @@ _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
+    "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_splits": (_i, [_i, _i, _i, _i]),
     "attn_device_status": (_i, [_vp]),
     "attn_last_error": (ctypes.c_char_p, []),
@@ -179,6 +180,26 @@ def attn_decode(q, kcache, vcache, out=None, kv_len=None, stream=None):
     return out
 
 
+def attn_decode_noalloc(q, kcache, vcache, out, kv_len=None, stream=None):
+    """attn_decode without any device allocation (see include/attn.h): the
+    caller supplies ``out``; the scratch is a fixed array inside the library."""
+    _check_tensor("q", q, 3)
+    _check_tensor("kcache", kcache, 4)
+    _check_tensor("vcache", vcache, 4)
+    _check_tensor("out", out, 3)
+    B, H, D = q.shape
+    Skv = kcache.shape[2]
+    if tuple(kcache.shape) != (B, H, Skv, D) or tuple(vcache.shape) != (B, H, Skv, D):
+        raise ValueError("kcache and vcache must be (B, H, Skv, D) matching q")
+    if tuple(out.shape) != (B, H, D) or not (q.dtype == kcache.dtype == vcache.dtype == out.dtype):
+        raise ValueError("out must be (B, H, D) and every tensor must share q's dtype")
+    kl = _kv_len_arg(kv_len, B, q.device)
+    rc = lib().attn_decode_noalloc(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, Skv, D, _ptr(kl),
+                                   _dtype_code(q), _stream_handle(stream))
+    _check(rc)
+    return out
+
+
 def attn_decode_splits(B: int, H: int, Skv: int, D: int) -> int:
     return lib().attn_decode_splits(B, H, Skv, D)
 
@@ -198,7 +219,7 @@ def attn_release() -> None:
 
 
 __all__ = [
-    "attn_fwd", "attn_decode", "attn_decode_splits", "attn_device_status", "attn_release",
+    "attn_fwd", "attn_decode", "attn_decode_noalloc", "attn_decode_splits", "attn_device_status", "attn_release",
     "attn_last_error", "attn_selftest_wait_timeout", "lib", "AttnError", "SIGNATURES", "LIB_PATH",
     "ATTN_F32", "ATTN_BF16", "ATTN_OK", "ATTN_EINVAL", "ATTN_EUNSUPPORTED", "ATTN_ECUDA",
     "ATTN_ENOMEM", "ATTN_ETIMEOUT",

@@ -275,6 +275,48 @@ ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, 
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode launch");
 }
 
+ATTN_API int attn_decode_noalloc(const void *q, const void *kcache, const void *vcache, void *out, int B,
+                                 int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream) {
+    g_last_error[0] = '\0';
+    if (B < 1 || H < 1 || Skv < 0)
+        return fail(ATTN_EINVAL, "attn_decode_noalloc: need B >= 1, H >= 1, Skv >= 0 (got %d, %d, %d)", B, H, Skv);
+    if (!q || !out || (Skv > 0 && (!kcache || !vcache)))
+        return fail(ATTN_EINVAL, "attn_decode_noalloc: q, out and (for Skv > 0) kcache, vcache must not be NULL");
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16)
+        return fail(ATTN_EINVAL, "attn_decode_noalloc: unknown dtype %d", dtype);
+    if (D <= 0) return fail(ATTN_EINVAL, "attn_decode_noalloc: D must be positive (got %d)", D);
+    if (dtype != ATTN_BF16) return fail(ATTN_EUNSUPPORTED, "attn_decode_noalloc: only bf16 is implemented");
+    if (D != 64 && D != 128)
+        return fail(ATTN_EUNSUPPORTED, "attn_decode_noalloc: D = %d not supported (64 or 128)", D);
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
+        return fail(ATTN_EINVAL, "attn_decode_noalloc: q, kcache, vcache and out must be 16-byte aligned");
+    if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
+        return fail(ATTN_EINVAL, "attn_decode_noalloc: kv_len must be 4-byte aligned");
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh * (Skv > 1 ? Skv : 1) >= (1LL << 31) || bh >= (1LL << 31) / 64)
+        return fail(ATTN_EINVAL, "attn_decode_noalloc: B*H*Skv is too large");
+    const size_t qo_bytes = static_cast<size_t>(bh) * D * 2;
+    const size_t kv_bytes = static_cast<size_t>(bh) * Skv * D * 2;
+    if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, kcache, kv_bytes) ||
+        overlaps(out, qo_bytes, vcache, kv_bytes))
+        return fail(ATTN_EINVAL, "attn_decode_noalloc: out overlaps an input");
+    const int chunk = decode_chunk(B, H, Skv);
+    const int n_split = attn_decode_splits(B, H, Skv, D);
+    const size_t need = static_cast<size_t>(bh) * n_split * (D + 2) * sizeof(float);
+    if (need > kDecodeNoAllocScratchBytes)
+        return fail(ATTN_EINVAL,
+                    "attn_decode_noalloc: these sizes need %zu bytes of scratch; the library's fixed "
+                    "scratch holds %zu (use attn_decode, or fewer sequences per call)",
+                    need, kDecodeNoAllocScratchBytes);
+    int *status = nullptr;
+    int rc = status_word(&status);
+    if (rc) return rc;
+    DecodeArgs a{q, kcache, vcache, out, kv_len, B, H, Skv, D, 1.0f / sqrtf(static_cast<float>(D)),
+                 chunk, n_split, nullptr, nullptr, status, static_cast<cudaStream_t>(stream)};
+    cudaError_t e = launch_decode_noalloc(a);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_noalloc launch");
+}
+
 ATTN_API int attn_device_status(void *stream) {
     g_last_error[0] = '\0';
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

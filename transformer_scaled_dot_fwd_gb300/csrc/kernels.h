@@ -47,6 +47,13 @@ cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUt
 // bf16 split-KV decode: partial kernel then combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a);
 
+// Size of the library-static decode scratch used by attn_decode_noalloc.
+constexpr size_t kDecodeNoAllocScratchBytes = 32u << 20;
+
+// Decode with its partials in the library-static scratch (no allocation).
+// The caller has checked that the partials fit in kDecodeNoAllocScratchBytes.
+cudaError_t launch_decode_noalloc(DecodeArgs a);
+
 // One-warp kernel whose only wait can never complete: exercises the bounded
 // wait and the status word (attn_selftest_wait_timeout).
 cudaError_t launch_wait_timeout_probe(long long limit, int *status, cudaStream_t stream);
