@@ -130,6 +130,30 @@ def test_masked_positions_are_selected_out(gpu):
     assert_close(full[:, :, :300], ref[:, :, :300], torch.bfloat16, "rows before huge keys")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_scale_zero_with_poisoned_hidden_keys(gpu, D):
+    """scale = 0 and NaN/inf keys past kv_len: -inf * 0 would be NaN, so the
+    hidden columns must still come out as exact zero weights; the result is the
+    mean of the visible V rows (oracle pin 'uniform scores')."""
+    B, H, S = 3, 2, 300
+    lens = [77, 200, 300]
+    q = wl.random_tensors((B, H, S, D), 23, count=1)[0]
+    k, v = wl.random_tensors((B, H, S, D), 24, count=2)
+    for b, L in enumerate(lens):
+        k[b, :, L:] = float("nan")
+        k[b, :, L::5] = float("-inf")
+    kl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = attn.attn_fwd(q, k, v, scale=0.0, causal=True, kv_len=kl)
+    attn.attn_device_status()
+    kc = k.clone()
+    for b, L in enumerate(lens):
+        kc[b, :, L:] = 0  # the oracle never reads hidden keys; keep its input finite anyway
+    ref = oracle.attention(q.cpu(), kc.cpu(), v.cpu(), scale=0.0, causal=True,
+                           kv_len=np.array(lens, np.int32))
+    assert not torch.isnan(out).any()
+    assert_close(out, ref, torch.bfloat16, f"scale 0 poisoned D={D}")
+
+
 def test_no_write_outside_out(gpu):
     B, H, S, D = 1, 3, 257, 128
     q, k, v = wl.random_tensors((B, H, S, D), 30)

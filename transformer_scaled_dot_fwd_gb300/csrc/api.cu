@@ -108,7 +108,7 @@ int get_encode(EncodeTiledFn *fn) {
 }
 
 // (D, S, B*H) bf16 view of a (B, H, S, D) tensor; boxes of 64 x 128 x 1 with
-// 128-byte swizzle, out-of-range rows read as zero.
+// 128-byte swizzle.  Loads read out-of-range rows as zero; stores skip them.
 int make_map(CUtensorMap *map, const void *base, int D, int S, long long BH) {
     EncodeTiledFn encode;
     int rc = get_encode(&encode);
@@ -218,11 +218,11 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, in
         if (B > 65535 || H > 65535) return fail(ATTN_EINVAL, "attn_fwd: B and H must be <= 65535 for fp32");
         e = launch_prefill_f32(a);
     } else {
-        CUtensorMap tq, tk, tv;
+        CUtensorMap tq, tk, tv, to;
         if ((rc = make_map(&tq, q, D, Sq, bh)) || (rc = make_map(&tk, k, D, Skv, bh)) ||
-            (rc = make_map(&tv, v, D, Skv, bh)))
+            (rc = make_map(&tv, v, D, Skv, bh)) || (rc = make_map(&to, out, D, Sq, bh)))
             return rc;
-        e = launch_prefill_tc(a, tq, tk, tv);
+        e = launch_prefill_tc(a, tq, tk, tv, to);
     }
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd launch");
 }

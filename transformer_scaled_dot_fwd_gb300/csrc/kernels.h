@@ -42,7 +42,7 @@ cudaError_t launch_prefill_f32(const FwdArgs &a);
 // bf16 tcgen05 prefill (D in {64, 128}); tq/tk/tv are 3-D tensor maps over
 // (D, S, B*H) with 64 x 128 x 1 boxes and 128-byte swizzle.
 cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv);
+                              const CUtensorMap &tv, const CUtensorMap &to);
 
 // bf16 split-KV decode: partial kernel then combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a);

@@ -18,19 +18,23 @@
 //               in the order S0_0 S1_0 | PV0_j S0_{j+1} PV1_j S1_{j+1} | ...
 //               so each softmax warpgroup has two MMA slots to hide behind.
 //   warps 4-7   softmax for Q0, warps 8-11 for Q1: thread = query row = TMEM
-//               lane.  Load the 128 fp32 scores of the row, mask (only on
-//               tiles that cross the causal diagonal or the padding edge),
-//               online max/sum in log2 units, p = 2^(s*scale*log2e - m),
-//               write p as bf16 over the S columns for the TS MMA.  O is
+//               lane.  Load the 128 fp32 scores of the row, online max/sum in
+//               log2 units, p = 2^(s*scale*log2e - m), write p as bf16 over
+//               the S columns for the TS MMA.  Tiles that cross the causal
+//               diagonal or the padding edge take a separate masked path;
+//               the common path carries no masking instructions at all.  O is
 //               rescaled lazily, only when the running max grows by more
 //               than 2^8, so most tiles never touch O.
-//   epilogue    the same warps: O / l -> bf16 -> global; rows with no visible
-//               key and padded query rows are written as exact zeros.
+//   epilogue    the same warps: O / l -> bf16 into the tile's (now free) Q
+//               buffer, then TMA stores; rows with no visible key and padded
+//               query rows are written as exact zeros.
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
 // P_x aliases the first 64 columns of S_x.
 // KV tiles wholly above the causal diagonal or past kv_len are never loaded.
 #include "kernels.h"
 #include "ptx.cuh"
+
+#include <type_traits>
 
 namespace attn {
 namespace {
@@ -85,16 +89,33 @@ struct Bars {
 #ifdef ATTN_TRACE
 __device__ long long *g_trace_buf;
 __device__ int g_trace_ctas[4];
+__device__ unsigned long long *g_cta_log;  // per CTA: SM id, start, MMA-done and end global times
 extern "C" __attribute__((visibility("default"))) int attn_trace_set(long long *buf, const int *ctas) {
     cudaMemcpyToSymbol(g_trace_buf, &buf, sizeof buf);
     return static_cast<int>(cudaMemcpyToSymbol(g_trace_ctas, ctas, 4 * sizeof(int)));
 }
+extern "C" __attribute__((visibility("default"))) int attn_cta_log_set(unsigned long long *buf) {
+    return static_cast<int>(cudaMemcpyToSymbol(g_cta_log, &buf, sizeof buf));
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned sm_id() {
+    unsigned s;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+    return s;
+}
+#define CTA_LOG(slot)                                                               \
+    if (g_cta_log) g_cta_log[static_cast<size_t>(blockIdx.x) * 4 + (slot)] = (slot) == 0 ? sm_id() : global_ns();
 #define TRACE_SETUP(t0_smem)                                                        \
     int trace_slot = -1, trace_n = 0;                                               \
     for (int ts = 0; ts < 4; ++ts)                                                  \
         if (g_trace_ctas[ts] == static_cast<int>(blockIdx.x) && g_trace_buf) trace_slot = ts; \
     long long *trace_smem = reinterpret_cast<long long *>(smem + L::kBarOff + 512);           \
-    if (threadIdx.x == 0) t0_smem = clock64();
+    for (int ti = threadIdx.x; ti < kTraceRoles * kTraceEvents; ti += blockDim.x) trace_smem[ti] = 0; \
+    if (threadIdx.x == 0) { t0_smem = clock64(); CTA_LOG(0) CTA_LOG(1) }
 #define TRACE(role, code, t0)                                                       \
     do {                                                                            \
         if (trace_slot >= 0 && trace_n < kTraceEvents)                              \
@@ -110,6 +131,7 @@ extern "C" __attribute__((visibility("default"))) int attn_trace_set(long long *
 #define TRACE_SETUP(t0_smem)
 #define TRACE(role, code, t0)
 #define TRACE_FLUSH()
+#define CTA_LOG(slot)
 #endif
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -119,7 +141,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const int n_pairs) {
+                      const __grid_constant__ CUtensorMap to, const int n_pairs) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -314,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(&bars.mma_done);
             volatile int never = 0;
             mbar_wait(&bars.mma_done, 0, &never);
+            CTA_LOG(2)
         }
     } else if (warp < 4) {
         regs_dec<kRegsProducer>();  // warps 2-3: no role, registers go to the softmax warps
@@ -337,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool tr = lane == 0 && (quarter == 0);
         for (int j = 0; j < n; ++j) {
             if (tr) TRACE(2 + x, 200 + x * 10 + j * 1000, bars.t0);
-            if (!(ok = mbar_wait_warp(&bars.s_full[x], sp, &bars.abort))) break;
+            if (!(ok = mbar_wait_warp<32>(&bars.s_full[x], sp, &bars.abort))) break;
             if (tr) TRACE(2 + x, 201 + x * 10 + j * 1000, bars.t0);
             sp ^= 1;
             tc_fence_after();
@@ -349,21 +372,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 4; ++c) reg_fence32(s + c * 32);
 
             if (tr) TRACE(2 + x, 202 + x * 10 + j * 1000, bars.t0);
-            const int kbase = j * kBN;
-            const bool need_mask = __any_sync(0xffffffffu, kbase + kBN > lim);
+            // This row sees columns [0, t) of the tile.  On a tile that crosses
+            // the causal diagonal or the padding edge, each warp sorts its
+            // 32-column chunks into seen by all its rows, hidden from all of
+            // them (no max, no exp, P = 0) and partial (per-column select).
+            const int t = lim - j * kBN;
+            const bool need_mask = __any_sync(0xffffffffu, t < kBN);
+            int t_lo = kBN, t_hi = kBN;
             if (need_mask) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (kbase + c >= lim) s[c] = f2u(-INFINITY);
+                t_lo = __reduce_min_sync(0xffffffffu, t);
+                t_hi = __reduce_max_sync(0xffffffffu, t);
             }
+            auto hidden = [&](int c) { return t_hi <= 32 * c; };
             // row max over the tile: 8 chains of 3-input max
-            float m8[8];
+            auto tile_max = [&](auto masked) -> float {
+                float m8[8];
+                if constexpr (!decltype(masked)::value) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m8[e] = fmaxf(u2f(s[2 * e]), u2f(s[2 * e + 1]));
+                    for (int e = 0; e < 8; ++e) m8[e] = fmaxf(u2f(s[2 * e]), u2f(s[2 * e + 1]));
 #pragma unroll
-            for (int c = 16; c < 128; c += 2)
-                m8[(c / 2) % 8] = fmax3(m8[(c / 2) % 8], u2f(s[c]), u2f(s[c + 1]));
-            const float mraw = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+                    for (int c = 16; c < 128; c += 2)
+                        m8[(c / 2) % 8] = fmax3(m8[(c / 2) % 8], u2f(s[c]), u2f(s[c + 1]));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        if (hidden(c)) {
+                            m8[2 * c] = m8[2 * c + 1] = -INFINITY;
+                            continue;
+                        }
+                        if (t_lo < 32 * c + 32) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                if (32 * c + e >= t) s[32 * c + e] = f2u(-INFINITY);
+                        }
+                        float a0 = fmaxf(u2f(s[32 * c]), u2f(s[32 * c + 1]));
+                        float a1 = fmaxf(u2f(s[32 * c + 2]), u2f(s[32 * c + 3]));
+#pragma unroll
+                        for (int e = 4; e < 32; e += 4) {
+                            a0 = fmax3(a0, u2f(s[32 * c + e]), u2f(s[32 * c + e + 1]));
+                            a1 = fmax3(a1, u2f(s[32 * c + e + 2]), u2f(s[32 * c + e + 3]));
+                        }
+                        m8[2 * c] = a0;
+                        m8[2 * c + 1] = a1;
+                    }
+                }
+                return fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+            };
+            const float mraw = need_mask ? tile_max(std::true_type{}) : tile_max(std::false_type{});
             const float m_tile = mraw == -INFINITY ? -INFINITY : mraw * sl2;
             const float m_new = fmaxf(m_run, m_tile);
             const bool grow = m_new > m_run + kRescaleLog2;
@@ -390,21 +445,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float negm = m_run == -INFINITY ? 0.f : -m_run;
             const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(negm, negm);
             uint64_t l4[4] = {0, 0, 0, 0};  // packed partial row sums
+            // p = 2^(s*scale*log2e - m) for the 32 columns of chunk c, packed
+            // into 16 bf16 pairs.  A hidden column holds -inf, and 2^-inf is an
+            // exact zero unless scale == 0 (then -inf * 0 is NaN: select it).
+            auto exp_chunk = [&](int c, uint32_t *p, auto zero_scale) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // two halves of 64 keys -> 32 packed columns each
-                uint32_t p[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const uint64_t arg = ffma2(f2_pack(u2f(s[h * 64 + 2 * e]), u2f(s[h * 64 + 2 * e + 1])),
-                                               sl2x2, negmx2);
+                for (int e = 0; e < 16; ++e) {
+                    const int k0 = 32 * c + 2 * e;
+                    const uint64_t arg = ffma2(f2_pack(u2f(s[k0]), u2f(s[k0 + 1])), sl2x2, negmx2);
                     float p0 = ex2_approx(f2_lo(arg));
                     float p1 = ex2_approx(f2_hi(arg));
-                    if (need_mask) {  // exact zeros, also when scale == 0
-                        p0 = u2f(s[h * 64 + 2 * e]) == -INFINITY ? 0.f : p0;
-                        p1 = u2f(s[h * 64 + 2 * e + 1]) == -INFINITY ? 0.f : p1;
+                    if constexpr (decltype(zero_scale)::value) {
+                        p0 = u2f(s[k0]) == -INFINITY ? 0.f : p0;
+                        p1 = u2f(s[k0 + 1]) == -INFINITY ? 0.f : p1;
                     }
                     l4[e % 4] = fadd2(l4[e % 4], f2_pack(p0, p1));
                     p[e] = pack_bf16x2(p0, p1);
+                }
+            };
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // two halves of 64 keys -> 32 packed columns each
+                uint32_t p[32];
+                if (!need_mask) {
+                    exp_chunk(2 * h, p, std::false_type{});
+                    exp_chunk(2 * h + 1, p + 16, std::false_type{});
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c = 2 * h + cc;
+                        if (hidden(c)) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) p[16 * cc + e] = 0u;
+                        } else if (sl2 == 0.f) {
+                            exp_chunk(c, p + 16 * cc, std::true_type{});
+                        } else {
+                            exp_chunk(c, p + 16 * cc, std::false_type{});
+                        }
+                    }
                 }
                 tmem_st32(t_s + h * 32, p);
             }
@@ -419,38 +496,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tr) TRACE(2 + x, 205 + x * 10 + j * 1000, bars.t0);
         }
 
-        // ---- epilogue
+        // ---- epilogue: O / l -> bf16, staged in this tile's Q buffer in the
+        // same 128-byte-swizzled layout the loads use, then one TMA store per
+        // 64-column block.  The Q buffer is free: o_full completes after every
+        // earlier MMA, the last one reading Q_x included.
         if (tr) TRACE(2 + x, 290 + x, bars.t0);
         bool have_o = n > 0 && ok;
         if (have_o) {
             have_o = mbar_wait_warp(&bars.o_full[x], 0, &bars.abort);
             tc_fence_after();
         }
+        uint32_t o[D];
+        if (have_o) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(t_o + c * 32, o + c * 32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) reg_fence32(o + c * 32);
+        }
         const bool zero_row = !have_o || (a.kv_len && i >= Lb) || !(l > 0.f);
         const float inv = zero_row ? 0.f : 1.f / l;
-        __nv_bfloat16 *orow =
-            static_cast<__nv_bfloat16 *>(a.out) + (static_cast<size_t>(bh) * a.Sq + i) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32] = {};
-            if (have_o) {
-                tmem_ld32(t_o + c * 32, o);
-                tmem_ld_wait();
-                reg_fence32(o);
-            }
-            uint32_t pk[16];
+        const uint32_t stage = smem_u32(smem + x * L::kTileBytes) + r * 128;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float v0 = zero_row ? 0.f : u2f(o[2 * e]) * inv;
-                const float v1 = zero_row ? 0.f : u2f(o[2 * e + 1]) * inv;
-                pk[e] = pack_bf16x2(v0, v1);
-            }
-            if (i < a.Sq) {
-                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+        for (int c = 0; c < L::kSub; ++c) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            for (int k8 = 0; k8 < 8; ++k8) {  // 16-byte chunk k8 of the row's 128-byte block c
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = c * 64 + k8 * 8 + 2 * e;
+                    pk[e] = zero_row ? 0u : pack_bf16x2(u2f(o[col]) * inv, u2f(o[col + 1]) * inv);
+                }
+                st_shared_v4(stage + c * L::kBlockBytes + ((k8 ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
             }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1 + x, 128);
+        if (quarter == 0 && lane == 0) {
+#pragma unroll
+            for (int c = 0; c < L::kSub; ++c)
+                tma_store_3d(&to, smem + x * L::kTileBytes + c * L::kBlockBytes, c * 64,
+                             (pair * kQTiles + x) * kBM, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();  // the buffer must outlive the store's reads
         }
     }
 
@@ -458,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     TRACE_FLUSH();
+    if (threadIdx.x == 0) { CTA_LOG(3) }
     if (warp == 1) {
         tc_fence_after();
         __syncwarp();
@@ -468,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv) {
+                     const CUtensorMap &tv, const CUtensorMap &to) {
     using L = Layout<D>;
     const int n_qt = (a.Sq + kBM - 1) / kBM;
     const int n_pairs = (n_qt + kQTiles - 1) / kQTiles;
@@ -478,7 +567,7 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<D><<<static_cast<unsigned>(blocks), kThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv,
+    prefill_tc_kernel<D><<<static_cast<unsigned>(blocks), kThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv, to,
                                                                                              n_pairs);
     return cudaGetLastError();
 }
@@ -486,8 +575,8 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv) {
-    return a.D == 64 ? launch_t<64>(a, tq, tk, tv) : launch_t<128>(a, tq, tk, tv);
+                              const CUtensorMap &tv, const CUtensorMap &to) {
+    return a.D == 64 ? launch_t<64>(a, tq, tk, tv, to) : launch_t<128>(a, tq, tk, tv, to);
 }
 
 }  // namespace attn

@@ -81,12 +81,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
 
 // Warp-collective bounded wait: every lane polls, the outcome is uniform
 // across the warp (needed before .sync.aligned tcgen05 instructions).
+// kSleepNs > 0 backs off between polls, leaving issue slots to other warps of
+// the sub-partition.
+template <int kSleepNs = 0>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
                                                volatile int *abort) {
     const long long t0 = clock64();
     for (;;) {
         const bool ok = mbar_try_wait(bar, parity);
         if (__all_sync(0xffffffffu, ok)) return true;
+        if constexpr (kSleepNs > 0) __nanosleep(kSleepNs);
         int give_up = 0;
         if (lane_id() == 0) {
             give_up = *abort != 0;
@@ -118,6 +122,40 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+// 3-D tiled TMA store of one box from shared memory to global memory; rows
+// outside the tensor are not written.  Completes through the bulk async-group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src, int c0, int c1,
+                                             int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until every committed bulk store of this thread has finished reading
+// its shared-memory source.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA) before a barrier hands the buffer to a bulk store.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
 }
 
 // Contiguous bulk copy global -> shared (16-byte aligned, size multiple of 16).
