@@ -12,7 +12,9 @@
 // first warpgroup gives registers to the two softmax warpgroups):
 //   warp 0      TMA producer: Q0/Q1 once, then K_j, V_j into a ring of
 //               32 KB stages (128-byte swizzle, 64-column boxes).
-//   warp 1      allocates 512 TMEM columns; lane 0 issues every MMA:
+//   warp 1      allocates 512 TMEM columns, then runs the MMA role as a
+//               whole warp (uniform control flow, operands in the uniform
+//               datapath); one elected lane issues every MMA:
 //                 S_x = Q_x K_j^T        (SS: both operands in shared memory)
 //                 O_x += P_x V_j         (TS: P read from TMEM, V MN-major)
 //               in the order S0_0 S1_0 | PV0_j S0_{j+1} PV1_j S1_{j+1} | ...
@@ -244,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         regs_dec<kRegsProducer>();
-        if (lane == 0 && N > 0) {
+        if (N > 0) {  // the whole warp runs this role; one elected lane issues
             const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
             const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 1);
             // Base descriptors, built once: the K-step offsets only move the
@@ -259,22 +261,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t koff = ((kk / 4) * L::kBlockBytes + (kk % 4) * 32) >> 4;
-                    mma_ss(tmem + L::s_col(x), desc_add(da, koff), desc_add(db, koff), idesc_s, kk > 0);
+                    mma_ss_warp(tmem + L::s_col(x), desc_add(da, koff), desc_add(db, koff), idesc_s, kk > 0);
                 }
             };
             auto issue_pv = [&](int x, int slot, bool acc) {
                 const uint64_t db = desc_add(dv0, (slot * L::kTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts(tmem + L::o_col(x), tmem + L::s_col(x) + kk * 8, desc_add(db, (kk * 16 * 128) >> 4),
+                    mma_ts_warp(tmem + L::o_col(x), tmem + L::s_col(x) + kk * 8, desc_add(db, (kk * 16 * 128) >> 4),
                            idesc_o, (acc || kk > 0) ? 1u : 0u);
             };
             int consumed = 0;
             uint32_t pr[2] = {0, 0};
-            bool ok = mbar_wait(&bars.q_full, 0, &bars.abort);
+            bool ok = mbar_wait_warp(&bars.q_full, 0, &bars.abort);
             if (ok) {
                 const int kslot = consumed % L::kStages;
-                ok = mbar_wait(&bars.kv_full[kslot], (consumed / L::kStages) & 1, &bars.abort);
+                ok = mbar_wait_warp(&bars.kv_full[kslot], (consumed / L::kStages) & 1, &bars.abort);
                 ++consumed;
                 if (ok) {
                     tc_fence_after();
@@ -282,60 +284,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int x = 0; x < kQTiles; ++x)
                         if (n_kv[x] > 0) {
                             issue_s(x, kslot);
-                            tc_commit(&bars.s_full[x]);
+                            tc_commit_warp(&bars.s_full[x]);
                         }
-                    tc_commit(&bars.kv_empty[kslot]);
+                    tc_commit_warp(&bars.kv_empty[kslot]);
                 }
             }
             for (int j = 0; j < N && ok; ++j) {
                 TRACE(1, 100 + j * 1000, bars.t0);
                 const int vslot = consumed % L::kStages;
-                if (!(ok = mbar_wait(&bars.kv_full[vslot], (consumed / L::kStages) & 1, &bars.abort))) break;
+                if (!(ok = mbar_wait_warp(&bars.kv_full[vslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                 ++consumed;
                 tc_fence_after();
                 TRACE(1, 101 + j * 1000, bars.t0);
                 if (j < n_kv[0]) {
-                    if (!(ok = mbar_wait(&bars.p_ready[0], pr[0], &bars.abort))) break;
+                    if (!(ok = mbar_wait_warp(&bars.p_ready[0], pr[0], &bars.abort))) break;
                     TRACE(1, 102 + j * 1000, bars.t0);
                     pr[0] ^= 1;
                     tc_fence_after();
                     issue_pv(0, vslot, j > 0);
-                    if (j == n_kv[0] - 1) tc_commit(&bars.o_full[0]);
+                    TRACE(1, 105 + j * 1000, bars.t0);
+                    if (j == n_kv[0] - 1) tc_commit_warp(&bars.o_full[0]);
                 }
                 const bool next = j + 1 < N;
                 int nslot = 0;
                 if (next) {
                     nslot = consumed % L::kStages;
-                    if (!(ok = mbar_wait(&bars.kv_full[nslot], (consumed / L::kStages) & 1, &bars.abort))) break;
+                    if (!(ok = mbar_wait_warp(&bars.kv_full[nslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                     ++consumed;
                     tc_fence_after();
+                    TRACE(1, 108 + j * 1000, bars.t0);
                     if (j + 1 < n_kv[0]) {
                         issue_s(0, nslot);  // overwrites P0_j: PV0_j was issued first
-                        tc_commit(&bars.s_full[0]);
+                        tc_commit_warp(&bars.s_full[0]);
                     }
                 }
                 TRACE(1, 103 + j * 1000, bars.t0);
                 if (j < n_kv[1]) {
-                    if (!(ok = mbar_wait(&bars.p_ready[1], pr[1], &bars.abort))) break;
+                    if (!(ok = mbar_wait_warp(&bars.p_ready[1], pr[1], &bars.abort))) break;
                     TRACE(1, 104 + j * 1000, bars.t0);
                     pr[1] ^= 1;
                     tc_fence_after();
                     issue_pv(1, vslot, j > 0);
-                    if (j == n_kv[1] - 1) tc_commit(&bars.o_full[1]);
+                    TRACE(1, 106 + j * 1000, bars.t0);
+                    if (j == n_kv[1] - 1) tc_commit_warp(&bars.o_full[1]);
                 }
-                tc_commit(&bars.kv_empty[vslot]);
+                tc_commit_warp(&bars.kv_empty[vslot]);
                 if (next) {
                     if (j + 1 < n_kv[1]) {
                         issue_s(1, nslot);
-                        tc_commit(&bars.s_full[1]);
+                        TRACE(1, 107 + j * 1000, bars.t0);
+                        tc_commit_warp(&bars.s_full[1]);
                     }
-                    tc_commit(&bars.kv_empty[nslot]);
+                    tc_commit_warp(&bars.kv_empty[nslot]);
                 }
             }
             // every MMA must have finished before TMEM is released
-            tc_commit(&bars.mma_done);
+            tc_commit_warp(&bars.mma_done);
             volatile int never = 0;
-            mbar_wait(&bars.mma_done, 0, &never);
+            mbar_wait_warp(&bars.mma_done, 0, &never);
             CTA_LOG(2)
         }
     } else if (warp < 4) {
