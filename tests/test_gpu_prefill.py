@@ -185,6 +185,36 @@ def test_stream_argument(gpu):
     assert_close(out, ref, torch.bfloat16, "side stream")
 
 
+def test_concurrent_streams_and_repeated_launches(gpu):
+    """The persistent kernel hands out work through a device counter per
+    launch: launches running at the same time on two streams must each cover
+    their own problem, and back-to-back launches must start from a reset
+    counter (every launch here reuses counters that earlier launches drained)."""
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    q1, k1, v1 = wl.random_tensors((4, 8, 1024, 128), 41)
+    q2, k2, v2 = wl.random_tensors((3, 8, 768, 64), 42)
+    ref1 = attn.attn_fwd(q1, k1, v1, causal=True).clone()
+    ref2 = attn.attn_fwd(q2, k2, v2, causal=False).clone()
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(40):
+        with torch.cuda.stream(s1):
+            o1 = attn.attn_fwd(q1, k1, v1, causal=True, stream=s1)
+        with torch.cuda.stream(s2):
+            o2 = attn.attn_fwd(q2, k2, v2, causal=False, stream=s2)
+        outs.append((o1, o2))
+    s1.synchronize()
+    s2.synchronize()
+    attn.attn_device_status()
+    for o1, o2 in outs:
+        assert torch.equal(o1, ref1)
+        assert torch.equal(o2, ref2)
+    r1 = oracle.attention_rows(q1.cpu(), k1.cpu(), v1.cpu(), np.array([[0, 0, 5], [3, 7, 1023]], np.int64),
+                               causal=True)
+    got = torch.stack([ref1[0, 0, 5], ref1[3, 7, 1023]]).cpu()
+    assert_close(got, r1, torch.bfloat16, "two streams, spot rows")
+
+
 def _sampled_rows(w, kv_len, per_head=6, seed=0):
     rng = np.random.default_rng(seed)
     rows = []

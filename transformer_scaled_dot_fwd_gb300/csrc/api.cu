@@ -108,7 +108,7 @@ int get_encode(EncodeTiledFn *fn) {
 }
 
 // (D, S, B*H) bf16 view of a (B, H, S, D) tensor; boxes of 64 x 128 x 1 with
-// 128-byte swizzle.  Loads read out-of-range rows as zero; stores skip them.
+// 128-byte swizzle, out-of-range rows read as zero.
 int make_map(CUtensorMap *map, const void *base, int D, int S, long long BH) {
     EncodeTiledFn encode;
     int rc = get_encode(&encode);
@@ -212,17 +212,17 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, in
     int *status = nullptr;
     int rc = status_word(&status);
     if (rc) return rc;
-    FwdArgs a{q, k, v, out, kv_len, B, H, Sq, Skv, D, scale, causal, status, st};
+    FwdArgs a{q, k, v, out, kv_len, B, H, Sq, Skv, D, scale, causal, status, st, num_sms()};
     cudaError_t e;
     if (dtype == ATTN_F32) {
         if (B > 65535 || H > 65535) return fail(ATTN_EINVAL, "attn_fwd: B and H must be <= 65535 for fp32");
         e = launch_prefill_f32(a);
     } else {
-        CUtensorMap tq, tk, tv, to;
+        CUtensorMap tq, tk, tv;
         if ((rc = make_map(&tq, q, D, Sq, bh)) || (rc = make_map(&tk, k, D, Skv, bh)) ||
-            (rc = make_map(&tv, v, D, Skv, bh)) || (rc = make_map(&to, out, D, Sq, bh)))
+            (rc = make_map(&tv, v, D, Skv, bh)))
             return rc;
-        e = launch_prefill_tc(a, tq, tk, tv, to);
+        e = launch_prefill_tc(a, tq, tk, tv);
     }
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd launch");
 }

@@ -17,6 +17,7 @@ struct FwdArgs {
     int causal;
     int *status;            // device status word
     cudaStream_t stream;
+    int n_sm;               // streaming multiprocessors on the device
 };
 
 struct DecodeArgs {
@@ -42,7 +43,7 @@ cudaError_t launch_prefill_f32(const FwdArgs &a);
 // bf16 tcgen05 prefill (D in {64, 128}); tq/tk/tv are 3-D tensor maps over
 // (D, S, B*H) with 64 x 128 x 1 boxes and 128-byte swizzle.
 cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, const CUtensorMap &to);
+                              const CUtensorMap &tv);
 
 // bf16 split-KV decode: partial kernel then combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a);

@@ -7,11 +7,16 @@
 // scheme the pages name as FlashAttention ("Scaled dot-product attention with
 // masking", "The memory problem"), redesigned here for Blackwell.
 //
-// One CTA owns two 128-row query tiles (Q0, Q1) of one (b, h) and streams the
-// 128-key K/V tiles they need through shared memory.  Roles (12 warps; the
-// first warpgroup gives registers to the two softmax warpgroups):
-//   warp 0      TMA producer: Q0/Q1 once, then K_j, V_j into a ring of
-//               32 KB stages (128-byte swizzle, 64-column boxes).
+// Persistent kernel, one CTA per SM.  A work item is two 128-row query tiles
+// (Q0, Q1) of one (b, h); items are numbered longest-first (causal cost grows
+// with the row) and handed out by an atomic counter, so each SM takes the
+// next item when it is ready for it.  Roles (12 warps; the first warpgroup
+// gives registers to the two softmax warpgroups):
+//   warp 0      TMA producer: fetches the next item, publishes it to the other
+//               roles through a small ring in shared memory, loads Q0/Q1 as
+//               soon as the previous item's last S MMA on that buffer has
+//               completed, and streams K_j, V_j through a ring of 32 KB stages
+//               (128-byte swizzle, 64-column boxes).
 //   warp 1      allocates 512 TMEM columns, then runs the MMA role as a
 //               whole warp (uniform control flow, operands in the uniform
 //               datapath); one elected lane issues every MMA:
@@ -27,35 +32,34 @@
 //               the common path carries no masking instructions at all.  O is
 //               rescaled lazily, only when the running max grows by more
 //               than 2^8, so most tiles never touch O.
-//   epilogue    the same warps: O / l -> bf16 into the tile's (now free) Q
-//               buffer, then TMA stores; rows with no visible key and padded
-//               query rows are written as exact zeros.
+//   epilogue    the same warps: O / l -> bf16, transposed through a 4 KB
+//               per-warp buffer so that every global store writes whole
+//               128-byte lines; rows with no visible key and padded query
+//               rows are written as exact zeros.
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
 // P_x aliases the first 64 columns of S_x.
 // KV tiles wholly above the causal diagonal or past kv_len are never loaded.
 #include "kernels.h"
 #include "ptx.cuh"
 
-#include <type_traits>
+#include <atomic>
+#include <mutex>
 
 namespace attn {
 namespace {
 
 constexpr int kBM = 128;       // query rows per Q tile (one TMEM lane each)
 constexpr int kBN = 128;       // keys per K/V tile
-constexpr int kQTiles = 2;     // Q tiles per CTA
+constexpr int kQTiles = 2;     // Q tiles per work item
 constexpr int kThreads = 384;  // 12 warps
 constexpr uint32_t kRegsProducer = 64;   // warps 0-3 after setmaxnreg
 constexpr uint32_t kRegsSoftmax = 216;   // warps 4-11: 128*64 + 256*216 <= 384*168
 constexpr int kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
-#ifdef ATTN_TRACE
-constexpr int kTraceRoles = 4, kTraceEvents = 512;
-constexpr int kTraceBytes = kTraceRoles * kTraceEvents * 8;  // timeline probes (profiling builds)
-#else
-constexpr int kTraceBytes = 0;
-#endif
+constexpr int kItemRing = 4;          // work items in flight between the roles
+constexpr int kItemReaders = 32 + 256;  // MMA warp + both softmax warpgroups
+constexpr int kSchedSlots = 64;       // launches that may run at once with their own counter
 
 template <int D>
 struct Layout {
@@ -64,8 +68,10 @@ struct Layout {
     static constexpr int kTileBytes = kSub * kBlockBytes;  // 32 KB at D = 128
     static constexpr int kStages = D == 128 ? 4 : 8;       // K/V ring depth
     static constexpr int kRingOff = kQTiles * kTileBytes;
-    static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-    static constexpr int kSmemBytes = kBarOff + 512 + kTraceBytes + 1024;  // + barriers (+ probes) + slack
+    static constexpr int kStageBytes = 32 * 128;           // per softmax warp: 32 rows x 64 columns bf16
+    static constexpr int kStageOff = kRingOff + kStages * kTileBytes;
+    static constexpr int kBarOff = kStageOff + 8 * kStageBytes;
+    static constexpr int kSmemBytes = kBarOff + 512 + 1024;  // + barriers + alignment slack
     // TMEM column of S_x (and of P_x, which aliases it) and of O_x
     static __device__ __forceinline__ uint32_t s_col(int x) { return static_cast<uint32_t>(x) * 128u; }
     static __device__ __forceinline__ uint32_t o_col(int x) { return 256u + static_cast<uint32_t>(x) * D; }
@@ -73,25 +79,36 @@ struct Layout {
 
 struct Bars {
     long long t0;  // CTA start clock (timeline probes)
-    uint64_t q_full;
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
     uint64_t kv_full[8];
     uint64_t kv_empty[8];
     uint64_t s_full[2];
     uint64_t p_ready[2];
     uint64_t o_full[2];
+    uint64_t item_full[kItemRing];
+    uint64_t item_empty[kItemRing];
     uint64_t mma_done;
+    int item[kItemRing];  // published work items, -1 = no more work
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
+
+// Work counters, one pair per launch slot: [0] next item, [1] CTAs finished.
+// The last CTA of a launch resets both, so the next launch on the slot starts
+// from zero without a separate clearing step.
+__device__ unsigned int g_sched[kSchedSlots][2];
 
 // Timeline probes for profiling builds (compiled out unless ATTN_TRACE is
-// defined): in chosen CTAs, the TMA thread, the MMA thread and one thread of
-// each softmax warpgroup record (event, SM clock since CTA start) in shared
-// memory; the CTA copies its record to global memory when it finishes.
+// defined): in chosen CTAs, the TMA thread, the MMA warp and one thread of
+// each softmax warpgroup record (event, SM clock since CTA start) straight to
+// global memory; each CTA can also log its SM, start, MMA-done and end times.
 #ifdef ATTN_TRACE
+constexpr int kTraceRoles = 4, kTraceEvents = 2048;
 __device__ long long *g_trace_buf;
 __device__ int g_trace_ctas[4];
-__device__ unsigned long long *g_cta_log;  // per CTA: SM id, start, MMA-done and end global times
+__device__ unsigned long long *g_cta_log;
 extern "C" __attribute__((visibility("default"))) int attn_trace_set(long long *buf, const int *ctas) {
     cudaMemcpyToSymbol(g_trace_buf, &buf, sizeof buf);
     return static_cast<int>(cudaMemcpyToSymbol(g_trace_ctas, ctas, 4 * sizeof(int)));
@@ -115,35 +132,76 @@ __device__ __forceinline__ unsigned sm_id() {
     int trace_slot = -1, trace_n = 0;                                               \
     for (int ts = 0; ts < 4; ++ts)                                                  \
         if (g_trace_ctas[ts] == static_cast<int>(blockIdx.x) && g_trace_buf) trace_slot = ts; \
-    long long *trace_smem = reinterpret_cast<long long *>(smem + L::kBarOff + 512);           \
-    for (int ti = threadIdx.x; ti < kTraceRoles * kTraceEvents; ti += blockDim.x) trace_smem[ti] = 0; \
     if (threadIdx.x == 0) { t0_smem = clock64(); CTA_LOG(0) CTA_LOG(1) }
 #define TRACE(role, code, t0)                                                       \
     do {                                                                            \
         if (trace_slot >= 0 && trace_n < kTraceEvents)                              \
-            trace_smem[(role) * kTraceEvents + trace_n++] =                         \
+            g_trace_buf[(trace_slot * kTraceRoles + (role)) * kTraceEvents + trace_n++] = \
                 (static_cast<long long>(code) << 40) | (clock64() - (t0));          \
     } while (0)
-#define TRACE_FLUSH()                                                               \
-    if (trace_slot >= 0) {                                                          \
-        for (int ti = threadIdx.x; ti < kTraceRoles * kTraceEvents; ti += blockDim.x) \
-            g_trace_buf[trace_slot * kTraceRoles * kTraceEvents + ti] = trace_smem[ti]; \
-    }
 #else
 #define TRACE_SETUP(t0_smem)
 #define TRACE(role, code, t0)
-#define TRACE_FLUSH()
 #define CTA_LOG(slot)
 #endif
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
+// One work item: query tiles 2*pair and 2*pair + 1 of head bh.
+struct Item {
+    int pair, bh, Lb;
+    int n_kv[kQTiles];  // K/V tiles each query tile needs (0: tile empty or fully padded)
+    int N;              // max of n_kv
+};
+
+__device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_pairs) {
+    Item it;
+    const int BH = a.B * a.H;
+    it.pair = n_pairs - 1 - t / BH;
+    it.bh = t % BH;
+    const int b = it.bh / a.H;
+    it.Lb = a.Skv;
+    if (a.kv_len) it.Lb = min(max(a.kv_len[b], 0), a.Skv);
+    const int off = a.Skv - a.Sq;  // causal: key j visible from query i iff j <= i + off
+    it.N = 0;
+#pragma unroll
+    for (int x = 0; x < kQTiles; ++x) {
+        const int row0 = (it.pair * kQTiles + x) * kBM;
+        int n = 0;
+        if (row0 < a.Sq && !(a.kv_len && row0 >= it.Lb)) {
+            int last = min(a.Sq - 1, row0 + kBM - 1);
+            if (a.kv_len) last = min(last, it.Lb - 1);
+            const int hi = a.causal ? min(it.Lb, last + off + 1) : it.Lb;
+            n = (hi + kBN - 1) / kBN;
+        }
+        it.n_kv[x] = n;
+        it.N = max(it.N, n);
+    }
+    return it;
+}
+
+// Read the item published in ring slot k % kItemRing (warp-wide).  The slot
+// stays readable until the caller releases it.  Returns false on a timed-out
+// wait.
+__device__ __forceinline__ bool take_item(Bars &bars, int k, int *t) {
+    const int slot = k % kItemRing;
+    if (!mbar_wait_warp(&bars.item_full[slot], (k / kItemRing) & 1, &bars.abort)) return false;
+    *t = *static_cast<volatile int *>(&bars.item[slot]);
+    return true;
+}
+__device__ __forceinline__ int reread_item(Bars &bars, int k) {
+    return *static_cast<volatile int *>(&bars.item[k % kItemRing]);
+}
+__device__ __forceinline__ void release_item(Bars &bars, int k) {
+    mbar_arrive(&bars.item_empty[k % kItemRing]);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const __grid_constant__ CUtensorMap to, const int n_pairs) {
+                      const int n_pairs, const int n_items, unsigned int *sched) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -154,38 +212,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     TRACE_SETUP(bars.t0)
 
-    // ---- work unit: longest query-tile pairs first (causal cost grows with the row)
-    const int BH = a.B * a.H;
-    const int pair = n_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
-    const int bh = static_cast<int>(blockIdx.x) % BH;
-    const int b = bh / a.H;
-    int Lb = a.Skv;
-    if (a.kv_len) Lb = min(max(a.kv_len[b], 0), a.Skv);
-    const int off = a.Skv - a.Sq;  // causal: key j visible from query i iff j <= i + off
-    int n_kv[kQTiles];             // K/V tiles each Q tile needs
-#pragma unroll
-    for (int x = 0; x < kQTiles; ++x) {
-        const int row0 = (pair * kQTiles + x) * kBM;
-        n_kv[x] = 0;
-        if (row0 < a.Sq && !(a.kv_len && row0 >= Lb)) {
-            int last = min(a.Sq - 1, row0 + kBM - 1);
-            if (a.kv_len) last = min(last, Lb - 1);
-            const int hi = a.causal ? min(Lb, last + off + 1) : Lb;
-            n_kv[x] = (hi + kBN - 1) / kBN;
-        }
-    }
-    const int N = max(n_kv[0], n_kv[1]);
-
     if (threadIdx.x == 0) {
-        mbar_init(&bars.q_full, 1);
+        for (int x = 0; x < kQTiles; ++x) {
+            mbar_init(&bars.q_full[x], 1);
+            mbar_init(&bars.q_empty[x], 1);
+            mbar_init(&bars.s_full[x], 1);
+            mbar_init(&bars.p_ready[x], 128);
+            mbar_init(&bars.o_full[x], 1);
+        }
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(&bars.kv_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);
         }
-        for (int x = 0; x < kQTiles; ++x) {
-            mbar_init(&bars.s_full[x], 1);
-            mbar_init(&bars.p_ready[x], 128);
-            mbar_init(&bars.o_full[x], 1);
+        for (int s = 0; s < kItemRing; ++s) {
+            mbar_init(&bars.item_full[s], 1);
+            mbar_init(&bars.item_empty[s], kItemReaders);
         }
         mbar_init(&bars.mma_done, 1);
         bars.abort = 0;
@@ -203,107 +244,144 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ================================================================ TMA producer
         regs_dec<kRegsProducer>();
-        if (lane == 0 && N > 0) {
+        if (lane == 0) {
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
-            uint32_t qbytes = 0;
-#pragma unroll
-            for (int x = 0; x < kQTiles; ++x) qbytes += n_kv[x] > 0 ? L::kTileBytes : 0;
-            mbar_arrive_expect_tx(&bars.q_full, qbytes);
-#pragma unroll
-            for (int x = 0; x < kQTiles; ++x)
-                if (n_kv[x] > 0)
-#pragma unroll
-                    for (int c = 0; c < L::kSub; ++c)
-                        tma_load_3d(smem + x * L::kTileBytes + c * L::kBlockBytes, &tq, &bars.q_full,
-                                    c * 64, (pair * kQTiles + x) * kBM, bh);
-            int issued = 0;
+            uint32_t q_uses[kQTiles] = {0, 0};  // Q_x loads issued so far
+            int issued = 0;                     // K/V ring loads issued so far
             bool ok = true;
-            for (int j = 0; j < N && ok; ++j) {
-                for (int kv = 0; kv < 2; ++kv) {  // K_j, then V_j
-                    const int slot = issued % L::kStages;
-                    if (issued >= L::kStages &&
-                        !mbar_wait(&bars.kv_empty[slot], ((issued / L::kStages) - 1) & 1, &bars.abort)) {
-                        ok = false;
+            for (int k = 0; ok; ++k) {
+                // ---- fetch the next item and publish it to the other roles
+                const int slot = k % kItemRing;
+                if (k >= kItemRing &&
+                    !(ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, &bars.abort)))
+                    break;
+                int t = static_cast<int>(atomicAdd(sched, 1u));
+                if (t >= n_items) t = -1;
+                *static_cast<volatile int *>(&bars.item[slot]) = t;
+                mbar_arrive(&bars.item_full[slot]);
+                if (t < 0) break;
+                const Item it = decode_item(t, a, n_pairs);
+                TRACE(0, 400 + (k % 100) * 100000, bars.t0);
+                // ---- Q_x, once the previous item's last S MMA on the buffer has completed
+#pragma unroll
+                for (int x = 0; x < kQTiles; ++x) {
+                    if (it.n_kv[x] == 0) continue;
+                    if (q_uses[x] > 0 && !(ok = mbar_wait(&bars.q_empty[x], (q_uses[x] - 1) & 1, &bars.abort)))
                         break;
-                    }
-                    TRACE(0, 300 + kv + j * 1000, bars.t0);
-                    mbar_arrive_expect_tx(&bars.kv_full[slot], L::kTileBytes);
+                    mbar_arrive_expect_tx(&bars.q_full[x], L::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < L::kSub; ++c)
-                        tma_load_3d(ring + slot * L::kTileBytes + c * L::kBlockBytes, kv ? &tv : &tk,
-                                    &bars.kv_full[slot], c * 64, j * kBN, bh);
-                    ++issued;
+                        tma_load_3d(smem + x * L::kTileBytes + c * L::kBlockBytes, &tq, &bars.q_full[x], c * 64,
+                                    (it.pair * kQTiles + x) * kBM, it.bh);
+                    ++q_uses[x];
+                }
+                // ---- K_j, then V_j, through the ring
+                for (int j = 0; j < it.N && ok; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int s = issued % L::kStages;
+                        if (issued >= L::kStages &&
+                            !(ok = mbar_wait(&bars.kv_empty[s], ((issued / L::kStages) - 1) & 1, &bars.abort)))
+                            break;
+                        TRACE(0, 300 + kv + j * 1000 + (k % 100) * 100000, bars.t0);
+                        mbar_arrive_expect_tx(&bars.kv_full[s], L::kTileBytes);
+#pragma unroll
+                        for (int c = 0; c < L::kSub; ++c)
+                            tma_load_3d(ring + s * L::kTileBytes + c * L::kBlockBytes, kv ? &tv : &tk,
+                                        &bars.kv_full[s], c * 64, j * kBN, it.bh);
+                        ++issued;
+                    }
                 }
             }
             // never leave with copies still landing in shared memory
             volatile int never = 0;
-            mbar_wait(&bars.q_full, 0, &never);
+            for (int x = 0; x < kQTiles; ++x)
+                if (q_uses[x] > 0) mbar_wait(&bars.q_full[x], (q_uses[x] - 1) & 1, &never);
             for (int u = max(0, issued - L::kStages); u < issued; ++u)
                 mbar_wait(&bars.kv_full[u % L::kStages], (u / L::kStages) & 1, &never);
         }
     } else if (warp == 1) {
         // ================================================================ MMA issuer
         regs_dec<kRegsProducer>();
-        if (N > 0) {  // the whole warp runs this role; one elected lane issues
-            const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
-            const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 1);
-            // Base descriptors, built once: the K-step offsets only move the
-            // start-address field (low 14 bits, no carry below 256 KB).
-            const uint64_t dq[2] = {sdesc_sw128(smem_u32(smem), 16, 1024),
-                                    sdesc_sw128(smem_u32(smem) + L::kTileBytes, 16, 1024)};
-            const uint64_t dk0 = sdesc_sw128(smem_u32(ring), 16, 1024);
-            const uint64_t dv0 = sdesc_sw128(smem_u32(ring), L::kBlockBytes, 1024);
-            auto issue_s = [&](int x, int slot) {
-                const uint64_t da = dq[x];
-                const uint64_t db = desc_add(dk0, (slot * L::kTileBytes) >> 4);
+        const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0);
+        const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 1);
+        // Base descriptors, built once: the K-step offsets only move the
+        // start-address field (low 14 bits, no carry below 256 KB).
+        const uint64_t dq[2] = {sdesc_sw128(smem_u32(smem), 16, 1024),
+                                sdesc_sw128(smem_u32(smem) + L::kTileBytes, 16, 1024)};
+        const uint64_t dk0 = sdesc_sw128(smem_u32(ring), 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(smem_u32(ring), L::kBlockBytes, 1024);
+        auto issue_s = [&](int x, int slot) {
+            const uint64_t da = dq[x];
+            const uint64_t db = desc_add(dk0, (slot * L::kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = ((kk / 4) * L::kBlockBytes + (kk % 4) * 32) >> 4;
-                    mma_ss_warp(tmem + L::s_col(x), desc_add(da, koff), desc_add(db, koff), idesc_s, kk > 0);
-                }
-            };
-            auto issue_pv = [&](int x, int slot, bool acc) {
-                const uint64_t db = desc_add(dv0, (slot * L::kTileBytes) >> 4);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t koff = ((kk / 4) * L::kBlockBytes + (kk % 4) * 32) >> 4;
+                mma_ss_warp(tmem + L::s_col(x), desc_add(da, koff), desc_add(db, koff), idesc_s, kk > 0);
+            }
+        };
+        auto issue_pv = [&](int x, int slot, bool acc) {
+            const uint64_t db = desc_add(dv0, (slot * L::kTileBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    mma_ts_warp(tmem + L::o_col(x), tmem + L::s_col(x) + kk * 8, desc_add(db, (kk * 16 * 128) >> 4),
-                           idesc_o, (acc || kk > 0) ? 1u : 0u);
-            };
-            int consumed = 0;
-            uint32_t pr[2] = {0, 0};
-            bool ok = mbar_wait_warp(&bars.q_full, 0, &bars.abort);
-            if (ok) {
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts_warp(tmem + L::o_col(x), tmem + L::s_col(x) + kk * 8, desc_add(db, (kk * 16 * 128) >> 4),
+                            idesc_o, (acc || kk > 0) ? 1u : 0u);
+        };
+        int consumed = 0;  // K/V ring stages consumed so far
+        uint32_t q_uses[kQTiles] = {0, 0}, pr[kQTiles] = {0, 0};
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            int t;
+            if (!(ok = take_item(bars, k, &t))) break;
+            release_item(bars, k);
+            // Values read from memory are not provably warp-uniform; broadcast
+            // them from lane 0 so the MMA code keeps its operands and branches
+            // in the uniform datapath.
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t < 0) break;
+            Item it = decode_item(t, a, n_pairs);
+#pragma unroll
+            for (int x = 0; x < kQTiles; ++x) it.n_kv[x] = __shfl_sync(0xffffffffu, it.n_kv[x], 0);
+            it.N = __shfl_sync(0xffffffffu, it.N, 0);
+            const int N = it.N;
+            if (N == 0) continue;
+#pragma unroll
+            for (int x = 0; x < kQTiles; ++x) {
+                if (it.n_kv[x] == 0) continue;
+                if (!(ok = mbar_wait_warp(&bars.q_full[x], q_uses[x] & 1, &bars.abort))) break;
+                ++q_uses[x];
+            }
+            if (!ok) break;
+            {
                 const int kslot = consumed % L::kStages;
-                ok = mbar_wait_warp(&bars.kv_full[kslot], (consumed / L::kStages) & 1, &bars.abort);
+                if (!(ok = mbar_wait_warp(&bars.kv_full[kslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                 ++consumed;
-                if (ok) {
-                    tc_fence_after();
+                tc_fence_after();
 #pragma unroll
-                    for (int x = 0; x < kQTiles; ++x)
-                        if (n_kv[x] > 0) {
-                            issue_s(x, kslot);
-                            tc_commit_warp(&bars.s_full[x]);
-                        }
-                    tc_commit_warp(&bars.kv_empty[kslot]);
-                }
+                for (int x = 0; x < kQTiles; ++x)
+                    if (it.n_kv[x] > 0) {
+                        issue_s(x, kslot);
+                        tc_commit_warp(&bars.s_full[x]);
+                        if (it.n_kv[x] == 1) tc_commit_warp(&bars.q_empty[x]);  // last read of Q_x
+                    }
+                tc_commit_warp(&bars.kv_empty[kslot]);
             }
             for (int j = 0; j < N && ok; ++j) {
-                TRACE(1, 100 + j * 1000, bars.t0);
+                TRACE(1, 100 + j * 1000 + (k % 100) * 100000, bars.t0);
                 const int vslot = consumed % L::kStages;
                 if (!(ok = mbar_wait_warp(&bars.kv_full[vslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                 ++consumed;
                 tc_fence_after();
-                TRACE(1, 101 + j * 1000, bars.t0);
-                if (j < n_kv[0]) {
+                TRACE(1, 101 + j * 1000 + (k % 100) * 100000, bars.t0);
+                if (j < it.n_kv[0]) {
                     if (!(ok = mbar_wait_warp(&bars.p_ready[0], pr[0], &bars.abort))) break;
-                    TRACE(1, 102 + j * 1000, bars.t0);
+                    TRACE(1, 102 + j * 1000 + (k % 100) * 100000, bars.t0);
                     pr[0] ^= 1;
                     tc_fence_after();
                     issue_pv(0, vslot, j > 0);
-                    TRACE(1, 105 + j * 1000, bars.t0);
-                    if (j == n_kv[0] - 1) tc_commit_warp(&bars.o_full[0]);
+                    TRACE(1, 105 + j * 1000 + (k % 100) * 100000, bars.t0);
+                    if (j == it.n_kv[0] - 1) tc_commit_warp(&bars.o_full[0]);
                 }
                 const bool next = j + 1 < N;
                 int nslot = 0;
@@ -312,38 +390,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait_warp(&bars.kv_full[nslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                     ++consumed;
                     tc_fence_after();
-                    TRACE(1, 108 + j * 1000, bars.t0);
-                    if (j + 1 < n_kv[0]) {
+                    TRACE(1, 108 + j * 1000 + (k % 100) * 100000, bars.t0);
+                    if (j + 1 < it.n_kv[0]) {
                         issue_s(0, nslot);  // overwrites P0_j: PV0_j was issued first
                         tc_commit_warp(&bars.s_full[0]);
+                        if (j + 2 == it.n_kv[0]) tc_commit_warp(&bars.q_empty[0]);
                     }
                 }
-                TRACE(1, 103 + j * 1000, bars.t0);
-                if (j < n_kv[1]) {
+                TRACE(1, 103 + j * 1000 + (k % 100) * 100000, bars.t0);
+                if (j < it.n_kv[1]) {
                     if (!(ok = mbar_wait_warp(&bars.p_ready[1], pr[1], &bars.abort))) break;
-                    TRACE(1, 104 + j * 1000, bars.t0);
+                    TRACE(1, 104 + j * 1000 + (k % 100) * 100000, bars.t0);
                     pr[1] ^= 1;
                     tc_fence_after();
                     issue_pv(1, vslot, j > 0);
-                    TRACE(1, 106 + j * 1000, bars.t0);
-                    if (j == n_kv[1] - 1) tc_commit_warp(&bars.o_full[1]);
+                    TRACE(1, 106 + j * 1000 + (k % 100) * 100000, bars.t0);
+                    if (j == it.n_kv[1] - 1) tc_commit_warp(&bars.o_full[1]);
                 }
                 tc_commit_warp(&bars.kv_empty[vslot]);
                 if (next) {
-                    if (j + 1 < n_kv[1]) {
+                    if (j + 1 < it.n_kv[1]) {
                         issue_s(1, nslot);
-                        TRACE(1, 107 + j * 1000, bars.t0);
+                        TRACE(1, 107 + j * 1000 + (k % 100) * 100000, bars.t0);
                         tc_commit_warp(&bars.s_full[1]);
+                        if (j + 2 == it.n_kv[1]) tc_commit_warp(&bars.q_empty[1]);
                     }
                     tc_commit_warp(&bars.kv_empty[nslot]);
                 }
             }
-            // every MMA must have finished before TMEM is released
-            tc_commit_warp(&bars.mma_done);
-            volatile int never = 0;
-            mbar_wait_warp(&bars.mma_done, 0, &never);
-            CTA_LOG(2)
         }
+        // every MMA must have finished before TMEM is released
+        tc_commit_warp(&bars.mma_done);
+        volatile int never = 0;
+        mbar_wait_warp(&bars.mma_done, 0, &never);
+        CTA_LOG(2)
     } else if (warp < 4) {
         regs_dec<kRegsProducer>();  // warps 2-3: no role, registers go to the softmax warps
     } else {
@@ -352,48 +432,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = (warp - 4) / 4;
         const int quarter = warp % 4;  // TMEM lanes [32*quarter, 32*quarter + 32)
         const int r = quarter * 32 + lane;
-        const int i = (pair * kQTiles + x) * kBM + r;  // query row
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const uint32_t t_s = t_lane + L::s_col(x);
         const uint32_t t_o = t_lane + L::o_col(x);
-        const int n = n_kv[x];
-        const int lim = a.causal ? min(Lb, i + off + 1) : Lb;  // keys [0, lim) visible
         const float sl2 = a.scale * kLog2e;
-        float m_run = -INFINITY, l = 0.f;
-        uint32_t sp = 0;
+        const int off = a.Skv - a.Sq;
+        const uint32_t stage = smem_u32(smem + L::kStageOff + (warp - 4) * L::kStageBytes);
+        uint32_t sp = 0, o_uses = 0;
         bool ok = true;
-
         const bool tr = lane == 0 && (quarter == 0);
-        for (int j = 0; j < n; ++j) {
-            if (tr) TRACE(2 + x, 200 + x * 10 + j * 1000, bars.t0);
-            if (!(ok = mbar_wait_warp<32>(&bars.s_full[x], sp, &bars.abort))) break;
-            if (tr) TRACE(2 + x, 201 + x * 10 + j * 1000, bars.t0);
-            sp ^= 1;
-            tc_fence_after();
-            uint32_t s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, s + c * 32);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) reg_fence32(s + c * 32);
-
-            if (tr) TRACE(2 + x, 202 + x * 10 + j * 1000, bars.t0);
-            // This row sees columns [0, t) of the tile.  On a tile that crosses
-            // the causal diagonal or the padding edge, each warp sorts its
-            // 32-column chunks into seen by all its rows, hidden from all of
-            // them (no max, no exp, P = 0) and partial (per-column select).
-            const int t = lim - j * kBN;
-            const bool need_mask = __any_sync(0xffffffffu, t < kBN);
-            int t_lo = kBN, t_hi = kBN;
-            if (need_mask) {
-                t_lo = __reduce_min_sync(0xffffffffu, t);
-                t_hi = __reduce_max_sync(0xffffffffu, t);
+        for (int k = 0; ok; ++k) {
+            int item;
+            if (!(ok = take_item(bars, k, &item))) break;
+            if (item < 0) {
+                release_item(bars, k);
+                break;
             }
-            auto hidden = [&](int c) { return t_hi <= 32 * c; };
-            // row max over the tile: 8 chains of 3-input max
-            auto tile_max = [&](auto masked) -> float {
+            int n, lim;
+            {
+                const Item it = decode_item(item, a, n_pairs);
+                const int i = (it.pair * kQTiles + x) * kBM + r;  // query row
+                n = it.n_kv[x];
+                lim = a.causal ? min(it.Lb, i + off + 1) : it.Lb;  // keys [0, lim) visible
+            }
+            float m_run = -INFINITY, l = 0.f;
+
+            for (int j = 0; j < n; ++j) {
+                if (tr) TRACE(2 + x, 200 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
+                if (!(ok = mbar_wait_warp<32>(&bars.s_full[x], sp, &bars.abort))) break;
+                if (tr) TRACE(2 + x, 201 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
+                sp ^= 1;
+                tc_fence_after();
+                uint32_t s[128];
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, s + c * 32);
+                tmem_ld_wait();
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) reg_fence32(s + c * 32);
+
+                if (tr) TRACE(2 + x, 202 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
+                // This row sees columns [0, t) of the tile.  On a tile that crosses
+                // the causal diagonal or the padding edge, each warp sorts its
+                // 32-column chunks into seen by all its rows, hidden from all of
+                // them (no max, no exp, P = 0) and partial (per-column select).
+                const int t = lim - j * kBN;
+                const bool need_mask = __any_sync(0xffffffffu, t < kBN);
+                int t_lo = kBN, t_hi = kBN;
+                if (need_mask) {
+                    t_lo = __reduce_min_sync(0xffffffffu, t);
+                    t_hi = __reduce_max_sync(0xffffffffu, t);
+                }
+                // row max over the tile: 8 chains of 3-input max
                 float m8[8];
-                if constexpr (!decltype(masked)::value) {
+                if (!need_mask) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) m8[e] = fmaxf(u2f(s[2 * e]), u2f(s[2 * e + 1]));
 #pragma unroll
@@ -402,11 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        if (hidden(c)) {
+                        if (t_hi <= 32 * c) {  // hidden from every row of the warp
                             m8[2 * c] = m8[2 * c + 1] = -INFINITY;
                             continue;
                         }
-                        if (t_lo < 32 * c + 32) {
+                        if (t_lo < 32 * c + 32) {  // partial: hide columns >= t
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
                                 if (32 * c + e >= t) s[32 * c + e] = f2u(-INFINITY);
@@ -422,167 +513,221 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m8[2 * c + 1] = a1;
                     }
                 }
-                return fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
-            };
-            const float mraw = need_mask ? tile_max(std::true_type{}) : tile_max(std::false_type{});
-            const float m_tile = mraw == -INFINITY ? -INFINITY : mraw * sl2;
-            const float m_new = fmaxf(m_run, m_tile);
-            const bool grow = m_new > m_run + kRescaleLog2;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float factor = grow ? ex2_approx(m_run - m_new) : 1.f;
-                if (grow) {
-                    l *= factor;
-                    m_run = m_new;
-                }
-                if (j > 0) {  // O holds earlier tiles: bring it to the new max
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(t_o + c * 32, o);
-                        tmem_ld_wait();
-                        reg_fence32(o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * factor);
-                        tmem_st32(t_o + c * 32, o);
+                const float mraw = fmaxf(fmax3(m8[0], m8[1], m8[2]), fmax3(fmax3(m8[3], m8[4], m8[5]), m8[6], m8[7]));
+                const float m_tile = mraw == -INFINITY ? -INFINITY : mraw * sl2;
+                const float m_new = fmaxf(m_run, m_tile);
+                const bool grow = m_new > m_run + kRescaleLog2;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float factor = grow ? ex2_approx(m_run - m_new) : 1.f;
+                    if (grow) {
+                        l *= factor;
+                        m_run = m_new;
                     }
-                }
-            }
-            if (tr) TRACE(2 + x, 203 + x * 10 + j * 1000, bars.t0);
-            const float negm = m_run == -INFINITY ? 0.f : -m_run;
-            const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(negm, negm);
-            uint64_t l4[4] = {0, 0, 0, 0};  // packed partial row sums
-            // p = 2^(s*scale*log2e - m) for the 32 columns of chunk c, packed
-            // into 16 bf16 pairs.  A hidden column holds -inf, and 2^-inf is an
-            // exact zero unless scale == 0 (then -inf * 0 is NaN: select it).
-            auto exp_chunk = [&](int c, uint32_t *p, auto zero_scale) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int k0 = 32 * c + 2 * e;
-                    const uint64_t arg = ffma2(f2_pack(u2f(s[k0]), u2f(s[k0 + 1])), sl2x2, negmx2);
-                    float p0 = ex2_approx(f2_lo(arg));
-                    float p1 = ex2_approx(f2_hi(arg));
-                    if constexpr (decltype(zero_scale)::value) {
-                        p0 = u2f(s[k0]) == -INFINITY ? 0.f : p0;
-                        p1 = u2f(s[k0 + 1]) == -INFINITY ? 0.f : p1;
-                    }
-                    l4[e % 4] = fadd2(l4[e % 4], f2_pack(p0, p1));
-                    p[e] = pack_bf16x2(p0, p1);
-                }
-            };
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {  // two halves of 64 keys -> 32 packed columns each
-                uint32_t p[32];
-                if (!need_mask) {
-                    exp_chunk(2 * h, p, std::false_type{});
-                    exp_chunk(2 * h + 1, p + 16, std::false_type{});
-                } else {
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * h + cc;
-                        if (hidden(c)) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) p[16 * cc + e] = 0u;
-                        } else if (sl2 == 0.f) {
-                            exp_chunk(c, p + 16 * cc, std::true_type{});
-                        } else {
-                            exp_chunk(c, p + 16 * cc, std::false_type{});
+                    if (j > 0) {  // O holds earlier tiles: bring it to the new max
+    #pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            uint32_t o[32];
+                            tmem_ld32(t_o + c * 32, o);
+                            tmem_ld_wait();
+                            reg_fence32(o);
+    #pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = f2u(u2f(o[e]) * factor);
+                            tmem_st32(t_o + c * 32, o);
                         }
                     }
                 }
-                tmem_st32(t_s + h * 32, p);
-            }
-            {
-                const uint64_t l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
-                l += f2_lo(l2) + f2_hi(l2);
-            }
-            if (tr) TRACE(2 + x, 204 + x * 10 + j * 1000, bars.t0);
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(&bars.p_ready[x]);
-            if (tr) TRACE(2 + x, 205 + x * 10 + j * 1000, bars.t0);
-        }
-
-        // ---- epilogue: O / l -> bf16, staged in this tile's Q buffer in the
-        // same 128-byte-swizzled layout the loads use, then one TMA store per
-        // 64-column block.  The Q buffer is free: o_full completes after every
-        // earlier MMA, the last one reading Q_x included.
-        if (tr) TRACE(2 + x, 290 + x, bars.t0);
-        bool have_o = n > 0 && ok;
-        if (have_o) {
-            have_o = mbar_wait_warp(&bars.o_full[x], 0, &bars.abort);
-            tc_fence_after();
-        }
-        uint32_t o[D];
-        if (have_o) {
+                if (tr) TRACE(2 + x, 203 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
+                const float negm = m_run == -INFINITY ? 0.f : -m_run;
+                const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(negm, negm);
+                uint64_t l4[4] = {0, 0, 0, 0};  // packed partial row sums
+                // p = 2^(s*scale*log2e - m), packed into bf16 pairs over the S
+                // columns.  A hidden column holds -inf and 2^-inf is an exact
+                // zero, except when scale == 0 (-inf * 0 is NaN: select it).
+#define ATTN_EXP_PAIR(k0, pe, SELECT)                                                         \
+    {                                                                                         \
+        const uint64_t arg = ffma2(f2_pack(u2f(s[k0]), u2f(s[(k0) + 1])), sl2x2, negmx2);     \
+        float p0 = ex2_approx(f2_lo(arg));                                                    \
+        float p1 = ex2_approx(f2_hi(arg));                                                    \
+        if (SELECT) {                                                                         \
+            p0 = u2f(s[k0]) == -INFINITY ? 0.f : p0;                                          \
+            p1 = u2f(s[(k0) + 1]) == -INFINITY ? 0.f : p1;                                    \
+        }                                                                                     \
+        l4[(pe) % 4] = fadd2(l4[(pe) % 4], f2_pack(p0, p1));                                  \
+        p[pe] = pack_bf16x2(p0, p1);                                                          \
+    }
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(t_o + c * 32, o + c * 32);
-            tmem_ld_wait();
+                for (int h = 0; h < 2; ++h) {  // two halves of 64 keys -> 32 packed columns each
+                    uint32_t p[32];
+                    if (!need_mask) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) reg_fence32(o + c * 32);
-        }
-        const bool zero_row = !have_o || (a.kv_len && i >= Lb) || !(l > 0.f);
-        const float inv = zero_row ? 0.f : 1.f / l;
-        const uint32_t stage = smem_u32(smem + x * L::kTileBytes) + r * 128;
+                        for (int e = 0; e < 32; ++e) ATTN_EXP_PAIR(h * 64 + 2 * e, e, false)
+                    } else {
 #pragma unroll
-        for (int c = 0; c < L::kSub; ++c) {
+                        for (int cc = 0; cc < 2; ++cc) {
+                            const int c = 2 * h + cc;
+                            if (t_hi <= 32 * c) {  // hidden from every row of the warp
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) {  // 16-byte chunk k8 of the row's 128-byte block c
-                uint32_t pk[4];
+                                for (int e = 0; e < 16; ++e) p[16 * cc + e] = 0u;
+                            } else if (sl2 != 0.f) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = c * 64 + k8 * 8 + 2 * e;
-                    pk[e] = zero_row ? 0u : pack_bf16x2(u2f(o[col]) * inv, u2f(o[col + 1]) * inv);
+                                for (int e = 0; e < 16; ++e) ATTN_EXP_PAIR(32 * c + 2 * e, 16 * cc + e, false)
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) ATTN_EXP_PAIR(32 * c + 2 * e, 16 * cc + e, true)
+                            }
+                        }
+                    }
+                    tmem_st32(t_s + h * 32, p);
                 }
-                st_shared_v4(stage + c * L::kBlockBytes + ((k8 ^ (r & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+#undef ATTN_EXP_PAIR
+                {
+                    const uint64_t l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
+                    l += f2_lo(l2) + f2_hi(l2);
+                }
+                if (tr) TRACE(2 + x, 204 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars.p_ready[x]);
+                if (tr) TRACE(2 + x, 205 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
             }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1 + x, 128);
-        if (quarter == 0 && lane == 0) {
+
+
+            // ---- epilogue: O / l -> bf16.  Each warp transposes its 32 rows
+            // through its own buffer (64 columns per pass, 128-byte swizzled
+            // rows) so that each global store instruction writes four whole
+            // 128-byte row segments.
+            if (tr) TRACE(2 + x, 290 + x + (k % 100) * 100000, bars.t0);
+            bool have_o = n > 0 && ok;
+            if (have_o) {
+                have_o = mbar_wait_warp(&bars.o_full[x], o_uses & 1, &bars.abort);
+                tc_fence_after();
+                ok = have_o;
+            }
+            if (n > 0) ++o_uses;
+            // the item again, from its ring slot (nothing of it stays live through the tile loop)
+            const Item it = decode_item(reread_item(bars, k), a, n_pairs);
+            release_item(bars, k);
+            const int row0 = (it.pair * kQTiles + x) * kBM;
+            const int i = row0 + r;
+            const bool zero_row = !have_o || (a.kv_len && i >= it.Lb) || !(l > 0.f);
+            const float inv = zero_row ? 0.f : 1.f / l;
+            __nv_bfloat16 *obh = static_cast<__nv_bfloat16 *>(a.out) + static_cast<size_t>(it.bh) * a.Sq * D;
+            const int wrow0 = row0 + quarter * 32;  // first row of this warp
 #pragma unroll
-            for (int c = 0; c < L::kSub; ++c)
-                tma_store_3d(&to, smem + x * L::kTileBytes + c * L::kBlockBytes, c * 64,
-                             (pair * kQTiles + x) * kBM, bh);
-            bulk_commit_group();
-            bulk_wait_group_read0();  // the buffer must outlive the store's reads
+            for (int c = 0; c < L::kSub; ++c) {
+                // Columns [64c, 64c + 64) of this row.  Loaded unconditionally (TMEM
+                // of this CTA): without O the select below writes zeros.
+                uint32_t o[64];
+                {
+                    tmem_ld32(t_o + c * 64, o);
+                    tmem_ld32(t_o + c * 64 + 32, o + 32);
+                    tmem_ld_wait();
+                    reg_fence32(o);
+                    reg_fence32(o + 32);
+                }
+                __syncwarp();  // the previous pass has read the buffer back
+#pragma unroll
+                for (int k8 = 0; k8 < 8; ++k8) {  // 16-byte chunk k8 of this row's 64 columns
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = k8 * 8 + 2 * e;
+                        pk[e] = zero_row ? 0u : pack_bf16x2(u2f(o[col]) * inv, u2f(o[col + 1]) * inv);
+                    }
+                    st_shared_v4(stage + lane * 128 + ((k8 ^ (lane & 7)) << 4), pk[0], pk[1], pk[2], pk[3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int s4 = 0; s4 < 8; ++s4) {  // rows 4*s4 .. 4*s4 + 3, one 16-byte chunk per lane
+                    const int rr = 4 * s4 + (lane >> 3), ch = lane & 7;
+                    const uint4 v = ld_shared_v4(stage + rr * 128 + ((ch ^ (rr & 7)) << 4));
+                    const int row = wrow0 + rr;
+                    if (row < a.Sq)
+                        *reinterpret_cast<uint4 *>(obh + static_cast<size_t>(row) * D + c * 64 + ch * 8) = v;
+                }
+            }
+            if (tr) TRACE(2 + x, 299 + (k % 100) * 100000, bars.t0);
         }
     }
 
-    if (lane == 0 && warp >= 4 && warp % 4 == 0) TRACE(2 + (warp - 4) / 4, 299, bars.t0);
     tc_fence_before();
     __syncthreads();
-    TRACE_FLUSH();
     if (threadIdx.x == 0) { CTA_LOG(3) }
     if (warp == 1) {
         tc_fence_after();
         __syncwarp();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0 && bars.abort) report_timeout(a.status, 0x11);
+    if (threadIdx.x == 0) {
+        if (bars.abort) report_timeout(a.status, 0x11);
+        // Every producer of this launch has taken its last item once all CTAs
+        // have counted themselves here: the last one resets the slot.
+        __threadfence();
+        if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(sched, 0u);
+            atomicExch(sched + 1, 0u);
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_sched_mutex;
+unsigned int *g_sched_base[kMaxDevices];
+std::atomic<unsigned int> g_sched_turn{0};
+
+// Work counters for one launch: a slot of g_sched, taken round-robin, so that
+// launches running at the same time on other streams count separately.
+cudaError_t sched_slot(unsigned int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    unsigned int *base;
+    {
+        std::lock_guard<std::mutex> lock(g_sched_mutex);
+        if (!g_sched_base[dev]) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_sched);
+            if (e != cudaSuccess) return e;
+            g_sched_base[dev] = static_cast<unsigned int *>(p);
+        }
+        base = g_sched_base[dev];
+    }
+    *out = base + 2 * (g_sched_turn.fetch_add(1u) % kSchedSlots);
+    return cudaSuccess;
 }
 
 template <int D>
 cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, const CUtensorMap &to) {
+                     const CUtensorMap &tv) {
     using L = Layout<D>;
     const int n_qt = (a.Sq + kBM - 1) / kBM;
     const int n_pairs = (n_qt + kQTiles - 1) / kQTiles;
-    const long long blocks = static_cast<long long>(a.B) * a.H * n_pairs;
-    if (blocks <= 0) return cudaSuccess;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L::kSmemBytes);
+    const long long n_items = static_cast<long long>(a.B) * a.H * n_pairs;
+    if (n_items <= 0) return cudaSuccess;
+    if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    unsigned int *sched = nullptr;
+    cudaError_t e = sched_slot(&sched);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<D><<<static_cast<unsigned>(blocks), kThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv, to,
-                                                                                             n_pairs);
+    const long long sms = a.n_sm > 0 ? a.n_sm : 1;
+    const unsigned grid = static_cast<unsigned>(n_items < sms ? n_items : sms);
+    e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    prefill_tc_kernel<D><<<grid, kThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv, n_pairs,
+                                                                      static_cast<int>(n_items), sched);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                              const CUtensorMap &tv, const CUtensorMap &to) {
-    return a.D == 64 ? launch_t<64>(a, tq, tk, tv, to) : launch_t<128>(a, tq, tk, tv, to);
+                              const CUtensorMap &tv) {
+    return a.D == 64 ? launch_t<64>(a, tq, tk, tv) : launch_t<128>(a, tq, tk, tv);
 }
 
 }  // namespace attn
