@@ -50,11 +50,11 @@ def load(path: Optional[str] = None):
 
 def _bind(lib):
     vp, dp, i32p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), ctypes.c_void_p
-    lib.oracle_attention.restype = ctypes.c_int
-    lib.oracle_attention.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp] + [ctypes.c_int] * 6 + [
+    lib.oracle_attention_gqa.restype = ctypes.c_int
+    lib.oracle_attention_gqa.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp] + [ctypes.c_int] * 7 + [
         ctypes.c_double, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int]
-    lib.oracle_attention_rows.restype = ctypes.c_int
-    lib.oracle_attention_rows.argtypes = [vp, vp, vp, ctypes.c_int, dp] + [ctypes.c_int] * 6 + [
+    lib.oracle_attention_rows_gqa.restype = ctypes.c_int
+    lib.oracle_attention_rows_gqa.argtypes = [vp, vp, vp, ctypes.c_int, dp] + [ctypes.c_int] * 7 + [
         ctypes.c_double, ctypes.c_int, i32p, ctypes.c_int, vp, ctypes.c_longlong, ctypes.c_int]
     return lib
 
@@ -107,7 +107,9 @@ def _kv_len_array(kv_len, B):
 
 def attention(q, k, v, scale=None, causal=False, kv_len=None, query_padding=None,
               need_weights=False, nthreads=None, lib=None):
-    """Attention of (B, H, Sq, Dk), (B, H, Skv, Dk), (B, H, Skv, Dv) arrays.
+    """Attention of (B, H, Sq, Dk) queries against (B, Hkv, Skv, Dk) keys and
+    (B, Hkv, Skv, Dv) values, Hkv dividing H: query head h uses key/value head
+    h // (H // Hkv) (grouped-query attention; Hkv == H is multi-head attention).
 
     Returns out (B, H, Sq, Dv) float64, plus the (B, H, Sq, Skv) weights when
     ``need_weights``.  ``scale`` defaults to 1/sqrt(Dk).  ``query_padding``
@@ -123,8 +125,8 @@ def attention(q, k, v, scale=None, causal=False, kv_len=None, query_padding=None
     if qa.ndim != 4 or ka.ndim != 4 or va.ndim != 4:
         raise ValueError("q, k, v must be 4-D (B, H, S, D)")
     B, H, Sq, Dk = qa.shape
-    Skv, Dv = ka.shape[2], va.shape[3]
-    if ka.shape != (B, H, Skv, Dk) or va.shape[:3] != (B, H, Skv):
+    Hkv, Skv, Dv = ka.shape[1], ka.shape[2], va.shape[3]
+    if ka.shape != (B, Hkv, Skv, Dk) or va.shape[:3] != (B, Hkv, Skv) or Hkv < 1 or H % Hkv:
         raise ValueError("shape mismatch between q, k, v")
     if scale is None:
         scale = 1.0 / np.sqrt(Dk)
@@ -134,15 +136,15 @@ def attention(q, k, v, scale=None, causal=False, kv_len=None, query_padding=None
     out = np.zeros((B, H, Sq, Dv), dtype=np.float64)
     w = np.zeros((B, H, Sq, Skv), dtype=np.float64) if need_weights else None
     lib = lib or load()
-    rc = lib.oracle_attention(
+    rc = lib.oracle_attention_gqa(
         qa.ctypes.data, ka.ctypes.data, va.ctypes.data, dt,
         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
         w.ctypes.data_as(ctypes.POINTER(ctypes.c_double)) if w is not None else None,
-        B, H, Sq, Skv, Dk, Dv, float(scale), int(bool(causal)),
+        B, H, Hkv, Sq, Skv, Dk, Dv, float(scale), int(bool(causal)),
         kl.ctypes.data if kl is not None else None, int(bool(query_padding)),
         _threads(nthreads))
     if rc != 0:
-        raise ValueError("oracle_attention rejected its arguments")
+        raise ValueError("oracle_attention_gqa rejected its arguments")
     return (out, w) if need_weights else out
 
 
@@ -156,7 +158,7 @@ def attention_rows(q, k, v, rows, scale=None, causal=False, kv_len=None, query_p
     ka, _ = _as_storage(k)
     va, _ = _as_storage(v)
     B, H, Sq, Dk = qa.shape
-    Skv, Dv = ka.shape[2], va.shape[3]
+    Hkv, Skv, Dv = ka.shape[1], ka.shape[2], va.shape[3]
     if scale is None:
         scale = 1.0 / np.sqrt(Dk)
     kl = _kv_len_array(kv_len, B)
@@ -165,19 +167,19 @@ def attention_rows(q, k, v, rows, scale=None, causal=False, kv_len=None, query_p
     r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
     out = np.zeros((r.shape[0], Dv), dtype=np.float64)
     lib = lib or load()
-    rc = lib.oracle_attention_rows(
+    rc = lib.oracle_attention_rows_gqa(
         qa.ctypes.data, ka.ctypes.data, va.ctypes.data, dt,
         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
-        B, H, Sq, Skv, Dk, Dv, float(scale), int(bool(causal)),
+        B, H, Hkv, Sq, Skv, Dk, Dv, float(scale), int(bool(causal)),
         kl.ctypes.data if kl is not None else None, int(bool(query_padding)),
         r.ctypes.data, int(r.shape[0]), _threads(nthreads))
     if rc != 0:
-        raise ValueError("oracle_attention_rows rejected its arguments")
+        raise ValueError("oracle_attention_rows_gqa rejected its arguments")
     return out
 
 
 def decode(q, kcache, vcache, kv_len=None, scale=None, nthreads=None):
-    """Single-query decode: q (B, H, D) against a (B, H, Skv, D) cache.
+    """Single-query decode: q (B, H, D) against a (B, Hkv, Skv, D) cache.
 
     The query sees every cached key j < L_b ("Scaled dot-product attention with
     masking", "Adding the causal mask": no mask for seq_q = 1).  Returns (B, H, D).

@@ -154,37 +154,57 @@ static int check_dims(int B, int H, int Sq, int Skv, int Dk, int Dv, int dtype)
 }
 
 /*
- * Full attention.  q: (B,H,Sq,Dk)  k: (B,H,Skv,Dk)  v: (B,H,Skv,Dv)
+ * Grouped-query attention ("Attention from First Principles", section 5 "The
+ * full multi-head computation" and "MHA, GQA, MQA -- the KV cache lever";
+ * "Scaled dot-product attention with masking", "Grouped-query attention
+ * (GQA)"): q has H heads, k and v have Hkv heads, Hkv divides H, and query head
+ * h attends with key/value head h / (H / Hkv) -- the head the pages'
+ * repeat_interleave(H / Hkv) of K and V places at position h.  Hkv == H is
+ * ordinary multi-head attention, Hkv == 1 is multi-query attention.
+ *
+ * q: (B,H,Sq,Dk)  k: (B,Hkv,Skv,Dk)  v: (B,Hkv,Skv,Dv)
  * out: (B,H,Sq,Dv) doubles.  weights: (B,H,Sq,Skv) doubles or NULL.
  * kv_len: host int32[B] or NULL (all keys valid).  query_padding: 1 makes
  * query rows i >= L_b zero (self-attention prefill over right-padded
  * batches), 0 leaves them as computed (decode, cross-attention).
  * Returns 0, or -1 on a bad argument.
  */
-int oracle_attention(const void *q, const void *k, const void *v, int dtype, double *out,
-                     double *weights, int B, int H, int Sq, int Skv, int Dk, int Dv,
-                     double scale, int causal, const int32_t *kv_len, int query_padding,
-                     int nthreads)
+int oracle_attention_gqa(const void *q, const void *k, const void *v, int dtype, double *out,
+                         double *weights, int B, int H, int Hkv, int Sq, int Skv, int Dk, int Dv,
+                         double scale, int causal, const int32_t *kv_len, int query_padding,
+                         int nthreads)
 {
-    if (check_dims(B, H, Sq, Skv, Dk, Dv, dtype) || !out)
+    if (check_dims(B, H, Sq, Skv, Dk, Dv, dtype) || !out || Hkv <= 0 || H % Hkv)
         return -1;
+    const int G = H / Hkv;
     long long n_bh = (long long)B * H;
     long long p;
     (void)nthreads;
 #pragma omp parallel for schedule(dynamic) num_threads(nthreads > 0 ? nthreads : 1)
     for (p = 0; p < n_bh; p++) {
-        int b = (int)(p / H);
+        int b = (int)(p / H), h = (int)(p % H);
+        size_t pkv = (size_t)b * Hkv + h / G; /* the key/value head of query head h */
         int Lb = sequence_length(kv_len, b, Skv);
         double *s_row = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
         for (int i = 0; i < Sq; i++) {
             double *w_row = weights ? weights + ((size_t)p * Sq + i) * Skv : NULL;
-            attention_row(q, k, v, dtype, (size_t)p * Sq * Dk, (size_t)p * Skv * Dk,
-                          (size_t)p * Skv * Dv, i, Sq, Skv, Dk, Dv, scale, causal, Lb,
-                          query_padding, out + ((size_t)p * Sq + i) * Dv, w_row, s_row);
+            attention_row(q, k, v, dtype, (size_t)p * Sq * Dk, pkv * Skv * Dk, pkv * Skv * Dv, i, Sq,
+                          Skv, Dk, Dv, scale, causal, Lb, query_padding,
+                          out + ((size_t)p * Sq + i) * Dv, w_row, s_row);
         }
         free(s_row);
     }
     return 0;
+}
+
+/* Multi-head attention: the grouped form with one key/value head per query head. */
+int oracle_attention(const void *q, const void *k, const void *v, int dtype, double *out,
+                     double *weights, int B, int H, int Sq, int Skv, int Dk, int Dv,
+                     double scale, int causal, const int32_t *kv_len, int query_padding,
+                     int nthreads)
+{
+    return oracle_attention_gqa(q, k, v, dtype, out, weights, B, H, H, Sq, Skv, Dk, Dv, scale,
+                                causal, kv_len, query_padding, nthreads);
 }
 
 /*
@@ -192,29 +212,41 @@ int oracle_attention(const void *q, const void *k, const void *v, int dtype, dou
  * triples (b, h, i); out receives n_rows x Dv doubles in that order.  Used to
  * check outputs at full benchmark sizes one row at a time.
  */
-int oracle_attention_rows(const void *q, const void *k, const void *v, int dtype, double *out,
-                          int B, int H, int Sq, int Skv, int Dk, int Dv, double scale, int causal,
-                          const int32_t *kv_len, int query_padding, const int64_t *rows,
-                          long long n_rows, int nthreads)
+int oracle_attention_rows_gqa(const void *q, const void *k, const void *v, int dtype, double *out,
+                              int B, int H, int Hkv, int Sq, int Skv, int Dk, int Dv, double scale,
+                              int causal, const int32_t *kv_len, int query_padding,
+                              const int64_t *rows, long long n_rows, int nthreads)
 {
-    if (check_dims(B, H, Sq, Skv, Dk, Dv, dtype) || !out || (n_rows > 0 && !rows))
+    if (check_dims(B, H, Sq, Skv, Dk, Dv, dtype) || !out || (n_rows > 0 && !rows) || Hkv <= 0 ||
+        H % Hkv)
         return -1;
     for (long long r = 0; r < n_rows; r++) {
         int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
         if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= Sq)
             return -1;
     }
+    const int G = H / Hkv;
     long long r;
     (void)nthreads;
 #pragma omp parallel for schedule(dynamic) num_threads(nthreads > 0 ? nthreads : 1)
     for (r = 0; r < n_rows; r++) {
         int b = (int)rows[3 * r], h = (int)rows[3 * r + 1], i = (int)rows[3 * r + 2];
         size_t p = (size_t)b * H + h;
+        size_t pkv = (size_t)b * Hkv + h / G;
         int Lb = sequence_length(kv_len, b, Skv);
         double *s_row = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
-        attention_row(q, k, v, dtype, p * Sq * Dk, p * Skv * Dk, p * Skv * Dv, i, Sq, Skv, Dk,
+        attention_row(q, k, v, dtype, p * Sq * Dk, pkv * Skv * Dk, pkv * Skv * Dv, i, Sq, Skv, Dk,
                       Dv, scale, causal, Lb, query_padding, out + (size_t)r * Dv, NULL, s_row);
         free(s_row);
     }
     return 0;
+}
+
+int oracle_attention_rows(const void *q, const void *k, const void *v, int dtype, double *out,
+                          int B, int H, int Sq, int Skv, int Dk, int Dv, double scale, int causal,
+                          const int32_t *kv_len, int query_padding, const int64_t *rows,
+                          long long n_rows, int nthreads)
+{
+    return oracle_attention_rows_gqa(q, k, v, dtype, out, B, H, H, Sq, Skv, Dk, Dv, scale, causal,
+                                     kv_len, query_padding, rows, n_rows, nthreads);
 }

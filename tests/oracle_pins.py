@@ -276,6 +276,42 @@ def pin_key_padding_is_truncation(att):
     np.testing.assert_allclose(padded, trunc, rtol=0, atol=1e-13)
 
 
+def pin_grouped_query_matches_library(att):
+    """Grouped-query and multi-query attention: query head h uses key/value head
+    h // (H // Hkv), which is what the pages' K.repeat_interleave(H // Hkv,
+    dim=1) builds before ordinary attention ('Attention from First
+    Principles', section 5 "The full multi-head computation"; 'Scaled
+    dot-product attention with masking', "Grouped-query attention (GQA)").
+    Checked against PyTorch's scaled_dot_product_attention in float64 on the
+    explicitly repeated keys and values."""
+    cases = [  # (B, H, Hkv, Sq, Skv, D, causal, kv_len)
+        (2, 6, 2, 5, 5, 8, True, None),
+        (2, 4, 1, 1, 9, 6, False, [9, 4]),        # multi-query decode with key padding
+        (1, 6, 3, 4, 7, 4, True, None),           # chunk of queries, three groups of two
+        (2, 8, 4, 6, 6, 5, True, [6, 3]),
+    ]
+    for n, (B, H, Hkv, Sq, Skv, D, causal, kl) in enumerate(cases):
+        q = _rand((B, H, Sq, D), 80 + n)
+        k, v = _rand((B, Hkv, Skv, D), 90 + n), _rand((B, Hkv, Skv, D), 100 + n)
+        G = H // Hkv
+        kr, vr = np.repeat(k, G, axis=1), np.repeat(v, G, axis=1)  # repeat_interleave on dim 1
+        allowed = np.ones((B, 1, Sq, Skv), dtype=bool)
+        ii, jj = np.arange(Sq)[:, None], np.arange(Skv)[None, :]
+        if causal:
+            allowed &= (jj <= ii + (Skv - Sq))[None, None]
+        if kl is not None:
+            allowed &= (jj[None] < np.array(kl)[:, None, None])[:, None]
+        scale = 1.0 / math.sqrt(D)
+        ref = _torch_sdpa_f64(q, kr, vr, allowed, scale)
+        out = att(q, k, v, scale=scale, causal=causal,
+                  kv_len=None if kl is None else np.array(kl, np.int32), query_padding=False)
+        ok = allowed.any(-1)
+        for b in range(B):
+            for i in range(Sq):
+                if ok[b, 0, i]:
+                    np.testing.assert_allclose(out[b, :, i], ref[b, :, i], rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_tiny_example_causal,
     pin_kube_dojo_example,
@@ -291,4 +327,5 @@ ALL_PINS = [
     pin_decode_equals_last_causal_row,
     pin_chunk_against_cache,
     pin_key_padding_is_truncation,
+    pin_grouped_query_matches_library,
 ]

@@ -71,6 +71,7 @@ MUTANTS = {
                             "for (d = 0; d < Dk - 1; d++)\n            dot +="),
     "padded_queries_kept": ("if (query_padding && i >= Lb)\n        return;",
                             "if (query_padding && i >= Lb && 0)\n        return;"),
+    "kv_head_by_modulo": ("size_t pkv = (size_t)b * Hkv + h / G;", "size_t pkv = (size_t)b * Hkv + h % Hkv;"),
     "keys_from_query_row": ("load_elem(k, dtype, k_bh + (size_t)j * Dk + d)",
                             "load_elem(k, dtype, k_bh + (size_t)(j < Sq ? j : 0) * Dk + d) * 0.0 + "
                             "load_elem(q, dtype, q_bh + (size_t)(j < Sq ? j : 0) * Dk + d)"),
