@@ -30,6 +30,18 @@ def test_rows_entry_matches_full():
     assert np.array_equal(got, want)
 
 
+def test_rows_entry_matches_full_grouped():
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((2, 6, 9, 4)).astype(np.float32)
+    k = rng.standard_normal((2, 2, 9, 4)).astype(np.float32)
+    v = rng.standard_normal((2, 2, 9, 4)).astype(np.float32)
+    kl = np.array([9, 5], np.int32)
+    full = oracle.attention(q, k, v, causal=True, kv_len=kl)
+    rows = np.array([[0, 0, 0], [0, 5, 8], [1, 3, 4], [1, 4, 7], [1, 1, 2]], np.int64)
+    got = oracle.attention_rows(q, k, v, rows, causal=True, kv_len=kl)
+    assert np.array_equal(got, full[rows[:, 0], rows[:, 1], rows[:, 2]])
+
+
 def test_bf16_inputs_are_widened_exactly():
     g = torch.Generator().manual_seed(4)
     q, k, v = (torch.randn(1, 2, 9, 8, generator=g).to(torch.bfloat16) for _ in range(3))
