@@ -97,6 +97,30 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, in
                       int dtype, void *stream);
 
 /*
+ * attn_fwd_gqa -- attn_fwd with grouped-query (or multi-query) attention.
+ *
+ * Defines: "Attention from First Principles", section 5 "The full
+ * multi-head computation" and "MHA, GQA, MQA -- the KV cache lever"; "Scaled
+ * dot-product attention with masking", "Grouped-query attention (GQA)": the
+ * keys and values have H_kv heads, H_kv divides H, and query head h attends
+ * with key/value head h / (H / H_kv) -- the head that repeating K and V
+ * H / H_kv times along the head axis (repeat_interleave) puts at position h.
+ * Nothing is repeated in memory.  H_kv == H is attn_fwd; H_kv == 1 is
+ * multi-query attention.
+ *
+ *   q    (B, H,    Sq,  D)
+ *   k    (B, H_kv, Skv, D)
+ *   v    (B, H_kv, Skv, D)
+ *   out  (B, H,    Sq,  D)  written; must not overlap q, k or v
+ *
+ * Every other argument, rule and error is as in attn_fwd; H_kv < 1 or H not
+ * a multiple of H_kv returns ATTN_EINVAL.
+ */
+ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out, int B, int H,
+                          int H_kv, int Sq, int Skv, int D, float scale, int causal,
+                          const int32_t *kv_len, int dtype, void *stream);
+
+/*
  * attn_decode -- one new query per (batch, head) against a KV cache.
  *
  * Defines: "Attention from First Principles", section 6 "Under the hood"

@@ -32,6 +32,7 @@ LIB_PATH = os.path.join(_HERE, "libattn.so")
 _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_splits": (_i, [_i, _i, _i, _i]),
@@ -130,16 +131,18 @@ def _kv_len_arg(kv_len, B, device):
 
 def attn_fwd(q, k, v, out=None, scale: Optional[float] = None, causal: bool = False,
              kv_len=None, stream=None):
-    """Prefill attention of (B, H, Sq, D) queries against (B, H, Skv, D) keys/values.
+    """Prefill attention of (B, H, Sq, D) queries against (B, H_kv, Skv, D)
+    keys/values, H_kv dividing H (H_kv < H: grouped-query attention, calls
+    attn_fwd_gqa).
 
     Returns ``out`` (allocated like q when not given).  See include/attn.h.
     """
     for name, t in (("q", q), ("k", k), ("v", v)):
         _check_tensor(name, t, 4)
     B, H, Sq, D = q.shape
-    Skv = k.shape[2]
-    if tuple(k.shape) != (B, H, Skv, D) or tuple(v.shape) != (B, H, Skv, D):
-        raise ValueError("k and v must be (B, H, Skv, D) matching q")
+    H_kv, Skv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, H_kv, Skv, D) or tuple(v.shape) != (B, H_kv, Skv, D) or H % H_kv:
+        raise ValueError("k and v must be (B, H_kv, Skv, D) matching q, with H_kv dividing H")
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
     if out is None:
@@ -150,8 +153,13 @@ def attn_fwd(q, k, v, out=None, scale: Optional[float] = None, causal: bool = Fa
     kl = _kv_len_arg(kv_len, B, q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Sq, Skv, D, float(scale),
-                        int(bool(causal)), _ptr(kl), _dtype_code(q), _stream_handle(stream))
+    if H_kv == H:
+        rc = lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Sq, Skv, D, float(scale),
+                            int(bool(causal)), _ptr(kl), _dtype_code(q), _stream_handle(stream))
+    else:
+        rc = lib().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, H_kv, Sq, Skv, D,
+                                float(scale), int(bool(causal)), _ptr(kl), _dtype_code(q),
+                                _stream_handle(stream))
     _check(rc)
     return out
 

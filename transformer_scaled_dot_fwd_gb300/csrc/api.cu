@@ -176,9 +176,17 @@ ATTN_API const char *attn_last_error(void) { return g_last_error; }
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H, int Sq,
                       int Skv, int D, float scale, int causal, const int32_t *kv_len, int dtype,
                       void *stream) {
+    return attn_fwd_gqa(q, k, v, out, B, H, H, Sq, Skv, D, scale, causal, kv_len, dtype, stream);
+}
+
+ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out, int B, int H,
+                          int H_kv, int Sq, int Skv, int D, float scale, int causal,
+                          const int32_t *kv_len, int dtype, void *stream) {
     g_last_error[0] = '\0';
     if (B < 1 || H < 1 || Sq < 0 || Skv < 0)
         return fail(ATTN_EINVAL, "attn_fwd: need B >= 1, H >= 1, Sq >= 0, Skv >= 0 (got %d, %d, %d, %d)", B, H, Sq, Skv);
+    if (H_kv < 1 || H % H_kv != 0)
+        return fail(ATTN_EINVAL, "attn_fwd: H_kv must divide H (got H = %d, H_kv = %d)", H, H_kv);
     if ((Sq > 0 && (!q || !out)) || (Skv > 0 && (!k || !v)))
         return fail(ATTN_EINVAL, "attn_fwd: q and out (Sq > 0), k and v (Skv > 0) must not be NULL");
     if (dtype != ATTN_F32 && dtype != ATTN_BF16) return fail(ATTN_EINVAL, "attn_fwd: unknown dtype %d", dtype);
@@ -197,8 +205,9 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, in
     if (rows >= (1LL << 31) || bh > 65535LL * 65535LL)
         return fail(ATTN_EINVAL, "attn_fwd: B*H*S = %lld rows is too large", rows);
     const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
+    const long long bh_kv = static_cast<long long>(B) * H_kv;
     const size_t q_bytes = static_cast<size_t>(bh) * Sq * D * esz;
-    const size_t kv_bytes = static_cast<size_t>(bh) * Skv * D * esz;
+    const size_t kv_bytes = static_cast<size_t>(bh_kv) * Skv * D * esz;
     if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||
         overlaps(out, q_bytes, v, kv_bytes))
         return fail(ATTN_EINVAL, "attn_fwd: out overlaps an input");
@@ -212,15 +221,15 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, in
     int *status = nullptr;
     int rc = status_word(&status);
     if (rc) return rc;
-    FwdArgs a{q, k, v, out, kv_len, B, H, Sq, Skv, D, scale, causal, status, st, num_sms()};
+    FwdArgs a{q, k, v, out, kv_len, B, H, Sq, Skv, D, scale, causal, status, st, num_sms(), H_kv};
     cudaError_t e;
     if (dtype == ATTN_F32) {
         if (B > 65535 || H > 65535) return fail(ATTN_EINVAL, "attn_fwd: B and H must be <= 65535 for fp32");
         e = launch_prefill_f32(a);
     } else {
         CUtensorMap tq, tk, tv;
-        if ((rc = make_map(&tq, q, D, Sq, bh)) || (rc = make_map(&tk, k, D, Skv, bh)) ||
-            (rc = make_map(&tv, v, D, Skv, bh)))
+        if ((rc = make_map(&tq, q, D, Sq, bh)) || (rc = make_map(&tk, k, D, Skv, bh_kv)) ||
+            (rc = make_map(&tv, v, D, Skv, bh_kv)))
             return rc;
         e = launch_prefill_tc(a, tq, tk, tv);
     }

@@ -18,6 +18,7 @@ struct FwdArgs {
     int *status;            // device status word
     cudaStream_t stream;
     int n_sm;               // streaming multiprocessors on the device
+    int H_kv;               // key/value heads (divides H); query head h reads head h / (H / H_kv)
 };
 
 struct DecodeArgs {

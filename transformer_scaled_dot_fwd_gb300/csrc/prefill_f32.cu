@@ -36,9 +36,10 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
     const int b = blockIdx.z, h = blockIdx.y;
     const int i = blockIdx.x * kRows + r;
     const size_t bh = static_cast<size_t>(b) * a.H + h;
+    const size_t bh_kv = static_cast<size_t>(b) * a.H_kv + h / (a.H / a.H_kv);  // grouped-query head
     const float *Q = static_cast<const float *>(a.q) + bh * a.Sq * D;
-    const float *K = static_cast<const float *>(a.k) + bh * a.Skv * D;
-    const float *V = static_cast<const float *>(a.v) + bh * a.Skv * D;
+    const float *K = static_cast<const float *>(a.k) + bh_kv * a.Skv * D;
+    const float *V = static_cast<const float *>(a.v) + bh_kv * a.Skv * D;
     float *O = static_cast<float *>(a.out) + bh * a.Sq * D;
 
     int L = a.Skv;

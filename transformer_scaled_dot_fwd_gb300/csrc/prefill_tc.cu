@@ -8,12 +8,15 @@
 // masking", "The memory problem"), redesigned here for Blackwell.
 //
 // Persistent kernel, one CTA per SM.  A work item is two 128-row query tiles
-// (Q0, Q1) of one (b, h); items are numbered longest-first (causal cost grows
-// with the row) and handed out by an atomic counter, so each SM takes the
-// next item when it is ready for it.  Roles (12 warps; the first warpgroup
-// gives registers to the two softmax warpgroups):
-//   warp 0      TMA producer: fetches the next item, publishes it to the other
-//               roles through a small ring in shared memory, loads Q0/Q1 as
+// (Q0, Q1) that read the same key/value head: two consecutive query tiles of
+// one head, or -- grouped-query attention with an even group size -- the same
+// query tile of two heads of one group.  Items are numbered longest-first
+// (causal cost grows with the row) and handed out by an atomic counter, so
+// each SM takes the next item when it is ready for it.  Roles (12 warps; the
+// first warpgroup gives registers to the two softmax warpgroups):
+//   warp 0      TMA producer: fetches and decodes the next item, publishes the
+//               record to the other roles through a small ring in shared
+//               memory, loads Q0/Q1 as
 //               soon as the previous item's last S MMA on that buffer has
 //               completed, and streams K_j, V_j through a ring of 32 KB stages
 //               (128-byte swizzle, 64-column boxes).
@@ -77,6 +80,21 @@ struct Layout {
     static __device__ __forceinline__ uint32_t o_col(int x) { return 256u + static_cast<uint32_t>(x) * D; }
 };
 
+// One work item: two 128-row query tiles that read the same key/value head.
+// Multi-head attention (and grouped-query attention with an odd group size)
+// pairs query tiles 2p and 2p + 1 of one head; grouped-query attention with an
+// even group size pairs query tile qt of heads 2m and 2m + 1 of one group, so
+// each K/V tile loaded into shared memory serves two heads.
+struct Item {
+    // Query tile x starts at row row_base + x * row_step of head bh_base + x * bh_step
+    // (b * H + h); scalars, so that a runtime x never indexes a local array.
+    int row_base, row_step, bh_base, bh_step;
+    int bh_kv;          // b * H_kv + h / G: the key/value head both tiles read
+    int Lb;
+    int n_kv[kQTiles];  // K/V tiles each query tile needs (0: tile empty or fully padded)
+    int N;              // max of n_kv
+};
+
 struct Bars {
     long long t0;  // CTA start clock (timeline probes)
     uint64_t q_full[2];
@@ -89,7 +107,7 @@ struct Bars {
     uint64_t item_full[kItemRing];
     uint64_t item_empty[kItemRing];
     uint64_t mma_done;
-    int item[kItemRing];  // published work items, -1 = no more work
+    Item item[kItemRing];  // published work items, decoded; N == -1: no more work
     uint32_t tmem_base;
     int abort;
 };
@@ -148,26 +166,42 @@ __device__ __forceinline__ unsigned sm_id() {
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-// One work item: query tiles 2*pair and 2*pair + 1 of head bh.
-struct Item {
-    int pair, bh, Lb;
-    int n_kv[kQTiles];  // K/V tiles each query tile needs (0: tile empty or fully padded)
-    int N;              // max of n_kv
-};
+__device__ __forceinline__ bool pairs_heads(const FwdArgs &a) { return ((a.H / a.H_kv) & 1) == 0; }
 
-__device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_pairs) {
+// n_major: query-tile pairs per head (tile pairing) or query tiles (head pairing).
+__device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_major) {
     Item it;
-    const int BH = a.B * a.H;
-    it.pair = n_pairs - 1 - t / BH;
-    it.bh = t % BH;
-    const int b = it.bh / a.H;
+    const int G = a.H / a.H_kv;
+    int b, h0;
+    if (pairs_heads(a)) {
+        const int HP = a.H / 2, BHP = a.B * HP;
+        const int qt = n_major - 1 - t / BHP;  // longest rows first
+        const int r = t % BHP;
+        b = r / HP;
+        h0 = 2 * (r % HP);
+        it.row_base = qt * kBM;
+        it.row_step = 0;
+        it.bh_base = b * a.H + h0;
+        it.bh_step = 1;
+    } else {
+        const int BH = a.B * a.H;
+        const int pair = n_major - 1 - t / BH;  // longest rows first
+        const int bh = t % BH;
+        b = bh / a.H;
+        h0 = bh % a.H;
+        it.row_base = pair * kQTiles * kBM;
+        it.row_step = kBM;
+        it.bh_base = bh;
+        it.bh_step = 0;
+    }
+    it.bh_kv = b * a.H_kv + h0 / G;
     it.Lb = a.Skv;
     if (a.kv_len) it.Lb = min(max(a.kv_len[b], 0), a.Skv);
     const int off = a.Skv - a.Sq;  // causal: key j visible from query i iff j <= i + off
     it.N = 0;
 #pragma unroll
     for (int x = 0; x < kQTiles; ++x) {
-        const int row0 = (it.pair * kQTiles + x) * kBM;
+        const int row0 = it.row_base + x * it.row_step;
         int n = 0;
         if (row0 < a.Sq && !(a.kv_len && row0 >= it.Lb)) {
             int last = min(a.Sq - 1, row0 + kBM - 1);
@@ -181,17 +215,42 @@ __device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_pairs
     return it;
 }
 
-// Read the item published in ring slot k % kItemRing (warp-wide).  The slot
-// stays readable until the caller releases it.  Returns false on a timed-out
-// wait.
-__device__ __forceinline__ bool take_item(Bars &bars, int k, int *t) {
+// The producer decodes each item once and publishes the record; the other
+// roles read it from the ring instead of repeating the integer divisions.
+__device__ __forceinline__ void publish_item(Bars &bars, int slot, const Item &it) {
+    volatile Item &d = bars.item[slot];
+    d.row_base = it.row_base;
+    d.row_step = it.row_step;
+    d.bh_base = it.bh_base;
+    d.bh_step = it.bh_step;
+    d.bh_kv = it.bh_kv;
+    d.Lb = it.Lb;
+    d.n_kv[0] = it.n_kv[0];
+    d.n_kv[1] = it.n_kv[1];
+    d.N = it.N;
+}
+__device__ __forceinline__ Item read_item(Bars &bars, int k) {
+    const volatile Item &sv = bars.item[k % kItemRing];
+    Item it;
+    it.row_base = sv.row_base;
+    it.row_step = sv.row_step;
+    it.bh_base = sv.bh_base;
+    it.bh_step = sv.bh_step;
+    it.bh_kv = sv.bh_kv;
+    it.Lb = sv.Lb;
+    it.n_kv[0] = sv.n_kv[0];
+    it.n_kv[1] = sv.n_kv[1];
+    it.N = sv.N;
+    return it;
+}
+// Wait (warp-wide) until the item in ring slot k % kItemRing is published and
+// read it.  The slot stays readable until the caller releases it.  Returns
+// false on a timed-out wait.
+__device__ __forceinline__ bool take_item(Bars &bars, int k, Item *it) {
     const int slot = k % kItemRing;
     if (!mbar_wait_warp(&bars.item_full[slot], (k / kItemRing) & 1, &bars.abort)) return false;
-    *t = *static_cast<volatile int *>(&bars.item[slot]);
+    *it = read_item(bars, k);
     return true;
-}
-__device__ __forceinline__ int reread_item(Bars &bars, int k) {
-    return *static_cast<volatile int *>(&bars.item[k % kItemRing]);
 }
 __device__ __forceinline__ void release_item(Bars &bars, int k) {
     mbar_arrive(&bars.item_empty[k % kItemRing]);
@@ -201,7 +260,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const int n_pairs, const int n_items, unsigned int *sched) {
+                      const int n_major, const int n_items, unsigned int *sched) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -257,12 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k >= kItemRing &&
                     !(ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, &bars.abort)))
                     break;
-                int t = static_cast<int>(atomicAdd(sched, 1u));
-                if (t >= n_items) t = -1;
-                *static_cast<volatile int *>(&bars.item[slot]) = t;
+                const int t = static_cast<int>(atomicAdd(sched, 1u));
+                Item it;
+                if (t < n_items) {
+                    it = decode_item(t, a, n_major);
+                } else {
+                    it = Item{0, 0, 0, 0, 0, 0, {0, 0}, -1};
+                }
+                publish_item(bars, slot, it);
                 mbar_arrive(&bars.item_full[slot]);
-                if (t < 0) break;
-                const Item it = decode_item(t, a, n_pairs);
+                if (it.N < 0) break;
                 TRACE(0, 400 + (k % 100) * 100000, bars.t0);
                 // ---- Q_x, once the previous item's last S MMA on the buffer has completed
 #pragma unroll
@@ -274,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < L::kSub; ++c)
                         tma_load_3d(smem + x * L::kTileBytes + c * L::kBlockBytes, &tq, &bars.q_full[x], c * 64,
-                                    (it.pair * kQTiles + x) * kBM, it.bh);
+                                    it.row_base + x * it.row_step, it.bh_base + x * it.bh_step);
                     ++q_uses[x];
                 }
                 // ---- K_j, then V_j, through the ring
@@ -289,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < L::kSub; ++c)
                             tma_load_3d(ring + s * L::kTileBytes + c * L::kBlockBytes, kv ? &tv : &tk,
-                                        &bars.kv_full[s], c * 64, j * kBN, it.bh);
+                                        &bars.kv_full[s], c * 64, j * kBN, it.bh_kv);
                         ++issued;
                     }
                 }
@@ -332,19 +395,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t q_uses[kQTiles] = {0, 0}, pr[kQTiles] = {0, 0};
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            int t;
-            if (!(ok = take_item(bars, k, &t))) break;
+            Item it;
+            if (!(ok = take_item(bars, k, &it))) break;
             release_item(bars, k);
             // Values read from memory are not provably warp-uniform; broadcast
             // them from lane 0 so the MMA code keeps its operands and branches
             // in the uniform datapath.
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (t < 0) break;
-            Item it = decode_item(t, a, n_pairs);
 #pragma unroll
             for (int x = 0; x < kQTiles; ++x) it.n_kv[x] = __shfl_sync(0xffffffffu, it.n_kv[x], 0);
             it.N = __shfl_sync(0xffffffffu, it.N, 0);
             const int N = it.N;
+            if (N < 0) break;
             if (N == 0) continue;
 #pragma unroll
             for (int x = 0; x < kQTiles; ++x) {
@@ -442,17 +503,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const bool tr = lane == 0 && (quarter == 0);
         for (int k = 0; ok; ++k) {
-            int item;
-            if (!(ok = take_item(bars, k, &item))) break;
-            if (item < 0) {
-                release_item(bars, k);
-                break;
-            }
             int n, lim;
             {
-                const Item it = decode_item(item, a, n_pairs);
-                const int i = (it.pair * kQTiles + x) * kBM + r;  // query row
-                n = it.n_kv[x];
+                Item it;
+                if (!(ok = take_item(bars, k, &it))) break;
+                if (it.N < 0) {
+                    release_item(bars, k);
+                    break;
+                }
+                const int i = it.row_base + x * it.row_step + r;  // query row
+                n = x ? it.n_kv[1] : it.n_kv[0];  // a select: x is not a compile-time index here
                 lim = a.causal ? min(it.Lb, i + off + 1) : it.Lb;  // keys [0, lim) visible
             }
             float m_run = -INFINITY, l = 0.f;
@@ -605,13 +665,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (n > 0) ++o_uses;
             // the item again, from its ring slot (nothing of it stays live through the tile loop)
-            const Item it = decode_item(reread_item(bars, k), a, n_pairs);
+            const Item it = read_item(bars, k);  // again: nothing of it stayed live through the tiles
             release_item(bars, k);
-            const int row0 = (it.pair * kQTiles + x) * kBM;
+            const int row0 = it.row_base + x * it.row_step;
             const int i = row0 + r;
             const bool zero_row = !have_o || (a.kv_len && i >= it.Lb) || !(l > 0.f);
             const float inv = zero_row ? 0.f : 1.f / l;
-            __nv_bfloat16 *obh = static_cast<__nv_bfloat16 *>(a.out) + static_cast<size_t>(it.bh) * a.Sq * D;
+            __nv_bfloat16 *obh = static_cast<__nv_bfloat16 *>(a.out) + static_cast<size_t>(it.bh_base + x * it.bh_step) * a.Sq * D;
             const int wrow0 = row0 + quarter * 32;  // first row of this warp
 #pragma unroll
             for (int c = 0; c < L::kSub; ++c) {
@@ -707,8 +767,10 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
                      const CUtensorMap &tv) {
     using L = Layout<D>;
     const int n_qt = (a.Sq + kBM - 1) / kBM;
-    const int n_pairs = (n_qt + kQTiles - 1) / kQTiles;
-    const long long n_items = static_cast<long long>(a.B) * a.H * n_pairs;
+    const bool head_pairs = ((a.H / a.H_kv) & 1) == 0;  // as pairs_heads()
+    const int n_major = head_pairs ? n_qt : (n_qt + kQTiles - 1) / kQTiles;
+    const long long n_items = head_pairs ? static_cast<long long>(a.B) * (a.H / 2) * n_qt
+                                         : static_cast<long long>(a.B) * a.H * n_major;
     if (n_items <= 0) return cudaSuccess;
     if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     unsigned int *sched = nullptr;
@@ -718,7 +780,7 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
     const unsigned grid = static_cast<unsigned>(n_items < sms ? n_items : sms);
     e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<D><<<grid, kThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv, n_pairs,
+    prefill_tc_kernel<D><<<grid, kThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv, n_major,
                                                                       static_cast<int>(n_items), sched);
     return cudaGetLastError();
 }
