@@ -325,6 +325,8 @@ def run_ours(args):
     w = wl.PREFILL
     if args.only == "decode":
         return run_decode_only(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
+    if args.only == "decode-gqa":
+        return run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
     q, k, v, kv_len = wl.prefill_inputs(w, device=device, seed=w.seed + 1000 * rank)
     out = torch.empty_like(q)
 
@@ -424,6 +426,50 @@ def decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, 
     return decode
 
 
+def run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
+    """Grouped-query decode on the decode workload's shape (B64 H32 D128, cache
+    padded to 8192, lengths U{4096..8192}) for H_kv in {32, 8, 1}: time, the
+    K/V bytes a step must read (sum_b 2*H_kv*L_b*D*2) and the flops (sum_b
+    4*H*L_b*D), so that flops / bytes = H / H_kv -- the intensity the pages
+    predict for grouped decode ('Attention from First Principles', section 6;
+    Exercise F).  One JSON line per H_kv; not part of the default run."""
+    dwk = wl.DECODE
+    B = args.decode_batch or dwk.B
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    lens = wl.draw_lengths(B, dwk.kv_len_range, dwk.seed + 1000 * rank).tolist()
+    kl = torch.tensor(lens, dtype=torch.int32, device=device)
+    for H_kv in (dwk.H, 8, 1):
+        g = torch.Generator(device=device).manual_seed(dwk.seed + H_kv)
+        q = torch.randn(B, dwk.H, dwk.D, device=device, generator=g).to(torch.bfloat16)
+        kc = torch.randn(B, H_kv, dwk.Skv, dwk.D, device=device, generator=g).to(torch.bfloat16)
+        vc = torch.randn(B, H_kv, dwk.Skv, dwk.D, device=device, generator=g).to(torch.bfloat16)
+        out = torch.empty_like(q)
+
+        def step():
+            attn.attn_decode(q, kc, vc, out=out, kv_len=kl)
+
+        for _ in range(args.warmup):
+            step()
+        attn.attn_device_status()
+        ms = time_steps(step, args.steps, stream, flush)
+        attn.attn_device_status()
+        avg = max_over_ranks(dist, float(sum(ms)), device) / args.steps
+        nbytes = decode_bytes(H_kv, dwk.D, lens)
+        flops = decode_flops(dwk.H, dwk.D, lens)
+        if rank == 0:
+            print(json.dumps({
+                "decode_gqa": {"workload": f"KV-cache decode B{B} H{dwk.H} H_kv{H_kv} D{dwk.D} Skv<={dwk.Skv} bf16",
+                               "ms_per_step": avg, "bytes_per_step": nbytes, "flops_per_step": flops,
+                               "intensity_flop_per_byte": flops / nbytes,
+                               "GB_per_s": nbytes / (avg * 1e-3) / 1e9,
+                               "hbm_frac": nbytes / (avg * 1e-3) / 1e9 / hbm_peak,
+                               "TFLOP_per_s": flops / (avg * 1e-3) / 1e12}}), flush=True)
+        del q, kc, vc, out
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_decode_only(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
     decode = decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
     if rank == 0:
@@ -474,7 +520,7 @@ def main():
                     help="approximate CPU time of the fp64 checker baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "decode-gqa"], default="all",
                     help="profiling runs: time one kernel family only")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="profiling runs: smaller decode batch than the workload's 64")

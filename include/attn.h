@@ -147,6 +147,29 @@ ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, 
                          int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream);
 
 /*
+ * attn_decode_gqa -- attn_decode with grouped-query (or multi-query) attention.
+ *
+ * Defines: as attn_decode, with the head grouping of attn_fwd_gqa: the cache
+ * has H_kv heads, H_kv divides H, and query head h attends with cached head
+ * h / (H / H_kv).  One read of a cached head serves all H / H_kv query heads
+ * of its group, which is why grouping raises decode's arithmetic intensity to
+ * about H / H_kv flops per byte ("Attention from First Principles", section 6
+ * "Under the hood").
+ *
+ *   q       (B, H, D)
+ *   kcache  (B, H_kv, Skv, D)
+ *   vcache  (B, H_kv, Skv, D)
+ *   out     (B, H, D)   written
+ *
+ * Every other argument, rule, error and the workspace behaviour are as in
+ * attn_decode; H_kv < 1 or H not a multiple of H_kv returns ATTN_EINVAL.
+ * H_kv == H runs attn_decode's kernels.
+ */
+ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcache, void *out, int B,
+                             int H, int H_kv, int Skv, int D, const int32_t *kv_len, int dtype,
+                             void *stream);
+
+/*
  * attn_decode_noalloc -- attn_decode that never allocates device memory.
  *
  * The pages have no counterpart: this entry point exists for callers that

@@ -99,3 +99,61 @@ def test_gqa_rejects_bad_grouping(gpu):
     rc = attn.lib().attn_fwd_gqa(P(q.data_ptr()), P(k.data_ptr()), P(k.data_ptr()), P(out.data_ptr()),
                                  1, 6, 4, 8, 8, 64, attn.ctypes.c_float(0.125), 1, None, 1, None)
     assert rc == attn.ATTN_EINVAL and "H_kv" in attn.attn_last_error()
+
+
+# ----------------------------------------------------------------- decode
+
+def _decode_case(B, H, H_kv, Skv, D, kv_len=None, seed=0):
+    q = wl.random_tensors((B, H, D), seed, count=1)[0]
+    kc, vc = wl.random_tensors((B, H_kv, Skv, D), seed + 1000, count=2)
+    kl = torch.tensor(kv_len, dtype=torch.int32, device="cuda") if kv_len is not None else None
+    out = attn.attn_decode(q, kc, vc, kv_len=kl)
+    attn.attn_device_status()
+    ref = oracle.decode(q.cpu(), kc.cpu(), vc.cpu(),
+                        kv_len=None if kv_len is None else np.array(kv_len, np.int32))
+    return q, kc, vc, out, ref
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("H,H_kv", [(8, 2), (8, 4), (6, 2), (12, 1), (32, 1), (32, 8)])
+@pytest.mark.parametrize("Skv", [1, 63, 65, 700, 3000])
+def test_gqa_decode(gpu, H, H_kv, Skv, D):
+    """Group sizes 2, 3, 4, 12 (a subgroup of 8 plus one of 4) and 32 (four
+    subgroups of 8), ragged chunk tails."""
+    _, _, _, out, ref = _decode_case(2, H, H_kv, Skv, D, seed=Skv + H + H_kv)
+    assert_close(out, ref, torch.bfloat16, f"decode H={H} H_kv={H_kv} Skv={Skv} D={D}")
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 2), (32, 1)])
+def test_gqa_decode_lengths(gpu, H, H_kv):
+    lens = [0, 1, 64, 65, 511, 512, 513, 2000]
+    _, _, _, out, ref = _decode_case(len(lens), H, H_kv, 2000, 128, kv_len=lens, seed=5)
+    assert_close(out, ref, torch.bfloat16, "grouped decode, per-sequence lengths")
+    assert torch.count_nonzero(out[0]) == 0
+
+
+def test_gqa_decode_equals_last_causal_row(gpu):
+    B, H, H_kv, S, D = 2, 8, 2, 300, 128
+    q = wl.random_tensors((B, H, S, D), 31, count=1)[0]
+    k, v = wl.random_tensors((B, H_kv, S, D), 32, count=2)
+    full = attn.attn_fwd(q, k, v, causal=True)
+    dec = attn.attn_decode(q[:, :, S - 1].contiguous(), k, v)
+    attn.attn_device_status()
+    assert_close(dec, full[:, :, S - 1].double().cpu().numpy(), torch.bfloat16, "decode vs last prefill row")
+
+
+def test_gqa_decode_full_size_sampled(gpu):
+    """The decode workload's shape with Llama-like grouping: B64 H32 H_kv8, cache
+    padded to 8192, lengths U{4096..8192}."""
+    w = wl.DECODE
+    B, H, H_kv, S, D = w.B, w.H, 8, w.Skv, w.D
+    g = torch.Generator(device="cuda").manual_seed(41)
+    q = torch.randn(B, H, D, device="cuda", generator=g).to(torch.bfloat16)
+    kc = torch.randn(B, H_kv, S, D, device="cuda", generator=g).to(torch.bfloat16)
+    vc = torch.randn(B, H_kv, S, D, device="cuda", generator=g).to(torch.bfloat16)
+    lens = torch.randint(4096, 8193, (B,), generator=torch.Generator().manual_seed(42), dtype=torch.int32)
+    out = attn.attn_decode(q, kc, vc, kv_len=lens.cuda())
+    attn.attn_device_status()
+    bs = [0, 1, 17, 63]
+    ref = oracle.decode(q[bs].cpu(), kc[bs].cpu(), vc[bs].cpu(), kv_len=lens[bs].numpy())
+    assert_close(out[bs], ref, torch.bfloat16, "B64 H32 H_kv8 decode, sampled sequences")

@@ -34,6 +34,7 @@ SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
+    "attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_splits": (_i, [_i, _i, _i, _i]),
     "attn_device_status": (_i, [_vp]),
@@ -165,7 +166,8 @@ def attn_fwd(q, k, v, out=None, scale: Optional[float] = None, causal: bool = Fa
 
 
 def attn_decode(q, kcache, vcache, out=None, kv_len=None, stream=None):
-    """One query per (batch, head): q (B, H, D) against a (B, H, Skv, D) cache.
+    """One query per (batch, head): q (B, H, D) against a (B, H_kv, Skv, D)
+    cache, H_kv dividing H (H_kv < H: grouped-query decode, attn_decode_gqa).
 
     Returns ``out`` (B, H, D).  See include/attn.h.
     """
@@ -173,17 +175,22 @@ def attn_decode(q, kcache, vcache, out=None, kv_len=None, stream=None):
     _check_tensor("kcache", kcache, 4)
     _check_tensor("vcache", vcache, 4)
     B, H, D = q.shape
-    Skv = kcache.shape[2]
-    if tuple(kcache.shape) != (B, H, Skv, D) or tuple(vcache.shape) != (B, H, Skv, D):
-        raise ValueError("kcache and vcache must be (B, H, Skv, D) matching q")
+    H_kv, Skv = kcache.shape[1], kcache.shape[2]
+    if (tuple(kcache.shape) != (B, H_kv, Skv, D) or tuple(vcache.shape) != (B, H_kv, Skv, D)
+            or H % H_kv):
+        raise ValueError("kcache and vcache must be (B, H_kv, Skv, D) matching q, with H_kv dividing H")
     if not (q.dtype == kcache.dtype == vcache.dtype):
         raise TypeError("q, kcache, vcache must share one dtype")
     if out is None:
         out = _torch().empty_like(q)
     _check_tensor("out", out, 3)
     kl = _kv_len_arg(kv_len, B, q.device)
-    rc = lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, Skv, D, _ptr(kl),
-                           _dtype_code(q), _stream_handle(stream))
+    if H_kv == H:
+        rc = lib().attn_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, Skv, D, _ptr(kl),
+                               _dtype_code(q), _stream_handle(stream))
+    else:
+        rc = lib().attn_decode_gqa(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), B, H, H_kv, Skv, D,
+                                   _ptr(kl), _dtype_code(q), _stream_handle(stream))
     _check(rc)
     return out
 

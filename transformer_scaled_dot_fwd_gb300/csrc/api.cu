@@ -156,6 +156,18 @@ int workspace(size_t bytes, void **out) {
     return ATTN_OK;
 }
 
+// Grouped-query decode: CTAs are (b, h_kv, head subgroup, chunk); the chunk
+// is at most kDecodeGqaMaxChunk keys (the kernel's score buffer).
+int decode_chunk_gqa(int B, int H, int H_kv, int Skv) {
+    const int G = H / H_kv;
+    const int gt = decode_gqa_heads_per_cta(G);
+    const long long units = static_cast<long long>(B) * H_kv * ((G + gt - 1) / gt);
+    const long long want = 6LL * num_sms();
+    int chunk = kDecodeGqaMaxChunk;
+    while (chunk > 64 && units * ((Skv + chunk - 1) / chunk) < want) chunk /= 2;
+    return chunk;
+}
+
 int decode_chunk(int B, int H, int Skv) {
     // Aim for at least ~6 CTAs per SM; shorter chunks only when the batch is small.
     const long long want = 6LL * num_sms();
@@ -245,9 +257,17 @@ ATTN_API int attn_decode_splits(int B, int H, int Skv, int D) {
 
 ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, void *out, int B,
                          int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream) {
+    return attn_decode_gqa(q, kcache, vcache, out, B, H, H, Skv, D, kv_len, dtype, stream);
+}
+
+ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcache, void *out, int B,
+                             int H, int H_kv, int Skv, int D, const int32_t *kv_len, int dtype,
+                             void *stream) {
     g_last_error[0] = '\0';
     if (B < 1 || H < 1 || Skv < 0)
         return fail(ATTN_EINVAL, "attn_decode: need B >= 1, H >= 1, Skv >= 0 (got %d, %d, %d)", B, H, Skv);
+    if (H_kv < 1 || H % H_kv != 0)
+        return fail(ATTN_EINVAL, "attn_decode: H_kv must divide H (got H = %d, H_kv = %d)", H, H_kv);
     if (!q || !out || (Skv > 0 && (!kcache || !vcache)))
         return fail(ATTN_EINVAL, "attn_decode: q, out and (for Skv > 0) kcache, vcache must not be NULL");
     if (dtype != ATTN_F32 && dtype != ATTN_BF16) return fail(ATTN_EINVAL, "attn_decode: unknown dtype %d", dtype);
@@ -259,16 +279,17 @@ ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, 
     if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
         return fail(ATTN_EINVAL, "attn_decode: kv_len must be 4-byte aligned");
     const long long bh = static_cast<long long>(B) * H;
+    const long long bh_kv = static_cast<long long>(B) * H_kv;
     if (bh * (Skv > 1 ? Skv : 1) >= (1LL << 31) || bh >= (1LL << 31) / 64)
         return fail(ATTN_EINVAL, "attn_decode: B*H*Skv is too large");
     const size_t qo_bytes = static_cast<size_t>(bh) * D * 2;
-    const size_t kv_bytes = static_cast<size_t>(bh) * Skv * D * 2;
+    const size_t kv_bytes = static_cast<size_t>(bh_kv) * Skv * D * 2;
     if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, kcache, kv_bytes) ||
         overlaps(out, qo_bytes, vcache, kv_bytes))
         return fail(ATTN_EINVAL, "attn_decode: out overlaps an input");
 
-    const int chunk = decode_chunk(B, H, Skv);
-    const int n_split = attn_decode_splits(B, H, Skv, D);
+    const int chunk = H_kv == H ? decode_chunk(B, H, Skv) : decode_chunk_gqa(B, H, H_kv, Skv);
+    const int n_split = Skv > 0 ? (Skv + chunk - 1) / chunk : 1;
     const size_t o_bytes = static_cast<size_t>(bh) * n_split * D * sizeof(float);
     const size_t ml_bytes = static_cast<size_t>(bh) * n_split * 2 * sizeof(float);
     void *ws = nullptr;
@@ -279,8 +300,8 @@ ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, 
     DecodeArgs a{q, kcache, vcache, out, kv_len, B, H, Skv, D, 1.0f / sqrtf(static_cast<float>(D)),
                  chunk, n_split, static_cast<float *>(ws),
                  reinterpret_cast<float *>(static_cast<char *>(ws) + o_bytes), status,
-                 static_cast<cudaStream_t>(stream)};
-    cudaError_t e = launch_decode(a);
+                 static_cast<cudaStream_t>(stream), H_kv};
+    cudaError_t e = H_kv == H ? launch_decode(a) : launch_decode_gqa(a);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode launch");
 }
 
@@ -321,7 +342,7 @@ ATTN_API int attn_decode_noalloc(const void *q, const void *kcache, const void *
     int rc = status_word(&status);
     if (rc) return rc;
     DecodeArgs a{q, kcache, vcache, out, kv_len, B, H, Skv, D, 1.0f / sqrtf(static_cast<float>(D)),
-                 chunk, n_split, nullptr, nullptr, status, static_cast<cudaStream_t>(stream)};
+                 chunk, n_split, nullptr, nullptr, status, static_cast<cudaStream_t>(stream), H};
     cudaError_t e = launch_decode_noalloc(a);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_noalloc launch");
 }

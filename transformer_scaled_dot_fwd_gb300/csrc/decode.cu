@@ -261,11 +261,20 @@ cudaError_t launch_decode_t(const DecodeArgs &a) {
     const long long blocks = static_cast<long long>(a.B) * a.H * a.n_split;
     if (a.Skv > 0)
         decode_partial_kernel<D><<<static_cast<unsigned>(blocks), kThreads, smem, a.stream>>>(a);
-    decode_combine_kernel<D><<<a.B * a.H, D, 0, a.stream>>>(a);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_decode_combine(a);
 }
 
 }  // namespace
+
+cudaError_t launch_decode_combine(const DecodeArgs &a) {
+    if (a.D == 64)
+        decode_combine_kernel<64><<<a.B * a.H, 64, 0, a.stream>>>(a);
+    else
+        decode_combine_kernel<128><<<a.B * a.H, 128, 0, a.stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_decode(const DecodeArgs &a) {
     return a.D == 64 ? launch_decode_t<64>(a) : launch_decode_t<128>(a);

@@ -34,9 +34,11 @@ struct DecodeArgs {
     float *part_ml;         // B*H*n_split*2 fp32 (running max in log2 units, sum)
     int *status;
     cudaStream_t stream;
+    int H_kv;               // cached heads (divides H); query head h reads head h / (H / H_kv)
 };
 
 constexpr int kDecodeMaxChunk = 1024;
+constexpr int kDecodeGqaMaxChunk = 512;
 
 // fp32 SIMT prefill (D in {64, 128}).
 cudaError_t launch_prefill_f32(const FwdArgs &a);
@@ -48,6 +50,15 @@ cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUt
 
 // bf16 split-KV decode: partial kernel then combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a);
+
+// The combine kernel alone (per query head: merge the chunk partials).
+cudaError_t launch_decode_combine(const DecodeArgs &a);
+
+// Grouped-query decode (H_kv < H): partial kernel per (b, h_kv, head subgroup,
+// chunk), then the combine kernel.  a.chunk must not exceed
+// kDecodeGqaMaxChunk (the kernel's score buffer holds that many keys).
+cudaError_t launch_decode_gqa(const DecodeArgs &a);
+int decode_gqa_heads_per_cta(int G);
 
 // Size of the library-static decode scratch used by attn_decode_noalloc.
 constexpr size_t kDecodeNoAllocScratchBytes = 32u << 20;
