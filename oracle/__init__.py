@@ -53,6 +53,9 @@ def _bind(lib):
     lib.oracle_attention_gqa.restype = ctypes.c_int
     lib.oracle_attention_gqa.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp] + [ctypes.c_int] * 7 + [
         ctypes.c_double, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int]
+    lib.oracle_attention_cache.restype = ctypes.c_int
+    lib.oracle_attention_cache.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp] + [ctypes.c_int] * 7 + [
+        ctypes.c_double, i32p, ctypes.c_int]
     lib.oracle_attention_rows_gqa.restype = ctypes.c_int
     lib.oracle_attention_rows_gqa.argtypes = [vp, vp, vp, ctypes.c_int, dp] + [ctypes.c_int] * 7 + [
         ctypes.c_double, ctypes.c_int, i32p, ctypes.c_int, vp, ctypes.c_longlong, ctypes.c_int]
@@ -106,7 +109,7 @@ def _kv_len_array(kv_len, B):
 
 
 def attention(q, k, v, scale=None, causal=False, kv_len=None, query_padding=None,
-              need_weights=False, nthreads=None, lib=None):
+              need_weights=False, nthreads=None, lib=None, cache_len=None, need_lse=False):
     """Attention of (B, H, Sq, Dk) queries against (B, Hkv, Skv, Dk) keys and
     (B, Hkv, Skv, Dv) values, Hkv dividing H: query head h uses key/value head
     h // (H // Hkv) (grouped-query attention; Hkv == H is multi-head attention).
@@ -116,6 +119,12 @@ def attention(q, k, v, scale=None, causal=False, kv_len=None, query_padding=None
     defaults to True when kv_len is given and Sq == Skv (self-attention
     prefill over a right-padded batch).  ``lib`` selects another build of
     oracle.c (the test suite uses it to run planted mistakes against the pins).
+
+    ``cache_len`` (int32[B]) or ``need_lse`` selects prefill of a chunk against
+    a KV cache instead: sequence b has cache_len[b] valid positions (all Skv
+    when None), query i sits at position cache_len[b] - Sq + i and sees keys up
+    to it (causal, no query padding); with ``need_lse`` the (B, H, Sq)
+    log-sum-exp of each row's visible scores is returned too.
     """
     qa, dt = _as_storage(q)
     ka, dt_k = _as_storage(k)
@@ -130,12 +139,27 @@ def attention(q, k, v, scale=None, causal=False, kv_len=None, query_padding=None
         raise ValueError("shape mismatch between q, k, v")
     if scale is None:
         scale = 1.0 / np.sqrt(Dk)
+    lib = lib or load()
+    if cache_len is not None or need_lse:
+        if kv_len is not None or need_weights or not causal:
+            raise ValueError("the cache form is causal and takes cache_len, not kv_len or weights")
+        cl = _kv_len_array(cache_len, B)
+        out = np.zeros((B, H, Sq, Dv), dtype=np.float64)
+        lse = np.zeros((B, H, Sq), dtype=np.float64)
+        rc = lib.oracle_attention_cache(
+            qa.ctypes.data, ka.ctypes.data, va.ctypes.data, dt,
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            lse.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            B, H, Hkv, Sq, Skv, Dk, Dv, float(scale), cl.ctypes.data if cl is not None else None,
+            _threads(nthreads))
+        if rc != 0:
+            raise ValueError("oracle_attention_cache rejected its arguments")
+        return (out, lse) if need_lse else out
     kl = _kv_len_array(kv_len, B)
     if query_padding is None:
         query_padding = kl is not None and Sq == Skv
     out = np.zeros((B, H, Sq, Dv), dtype=np.float64)
     w = np.zeros((B, H, Sq, Skv), dtype=np.float64) if need_weights else None
-    lib = lib or load()
     rc = lib.oracle_attention_gqa(
         qa.ctypes.data, ka.ctypes.data, va.ctypes.data, dt,
         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),

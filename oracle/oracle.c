@@ -66,12 +66,17 @@ static double load_elem(const void *base, int dtype, size_t idx)
     return (double)f;
 }
 
-/* Is key j visible from query i?  (readings 2 and 3 above) */
-static int key_visible(int i, int j, int Sq, int Skv, int causal, int Lb)
+/*
+ * Is key j visible from query i?  (readings 2 and 3 above)  `off` is the
+ * absolute position of query 0 among the keys: Skv - Sq when the last query
+ * is aligned with the last key, L_b - Sq for a chunk of queries at the end of
+ * a cached sequence of L_b positions.
+ */
+static int key_visible(int i, int j, int off, int causal, int Lb)
 {
     if (j >= Lb)
         return 0;
-    if (causal && j > i + (Skv - Sq))
+    if (causal && j > i + off)
         return 0;
     return 1;
 }
@@ -82,9 +87,9 @@ static int key_visible(int i, int j, int Sq, int Skv, int causal, int Lb)
  * attention weights of this row (zero for forbidden keys).
  */
 static void attention_row(const void *q, const void *k, const void *v, int dtype,
-                          size_t q_bh, size_t k_bh, size_t v_bh, int i, int Sq, int Skv,
+                          size_t q_bh, size_t k_bh, size_t v_bh, int i, int off, int Skv,
                           int Dk, int Dv, double scale, int causal, int Lb, int query_padding,
-                          double *out_row, double *w_row, double *s_row)
+                          double *out_row, double *w_row, double *s_row, double *lse)
 {
     int d, j;
     for (d = 0; d < Dv; d++)
@@ -93,6 +98,8 @@ static void attention_row(const void *q, const void *k, const void *v, int dtype
         for (j = 0; j < Skv; j++)
             w_row[j] = 0.0;
 
+    if (lse)
+        *lse = -INFINITY;
     /* reading 4: a padded query row is zero */
     if (query_padding && i >= Lb)
         return;
@@ -101,7 +108,7 @@ static void attention_row(const void *q, const void *k, const void *v, int dtype
     int any = 0;
     double m = 0.0;
     for (j = 0; j < Skv; j++) {
-        if (!key_visible(i, j, Sq, Skv, causal, Lb))
+        if (!key_visible(i, j, off, causal, Lb))
             continue;
         double dot = 0.0;
         for (d = 0; d < Dk; d++)
@@ -119,10 +126,13 @@ static void attention_row(const void *q, const void *k, const void *v, int dtype
     /* max-subtracted softmax over the key axis, then the mixture of V rows */
     double z = 0.0;
     for (j = 0; j < Skv; j++)
-        if (key_visible(i, j, Sq, Skv, causal, Lb))
+        if (key_visible(i, j, off, causal, Lb))
             z += exp(s_row[j] - m);
+    /* log-sum-exp of the visible scores: log(sum_j exp(s_j)) = m + log(z) */
+    if (lse)
+        *lse = m + log(z);
     for (j = 0; j < Skv; j++) {
-        if (!key_visible(i, j, Sq, Skv, causal, Lb))
+        if (!key_visible(i, j, off, causal, Lb))
             continue;
         double w = exp(s_row[j] - m) / z;
         if (w_row)
@@ -188,9 +198,9 @@ int oracle_attention_gqa(const void *q, const void *k, const void *v, int dtype,
         double *s_row = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
         for (int i = 0; i < Sq; i++) {
             double *w_row = weights ? weights + ((size_t)p * Sq + i) * Skv : NULL;
-            attention_row(q, k, v, dtype, (size_t)p * Sq * Dk, pkv * Skv * Dk, pkv * Skv * Dv, i, Sq,
-                          Skv, Dk, Dv, scale, causal, Lb, query_padding,
-                          out + ((size_t)p * Sq + i) * Dv, w_row, s_row);
+            attention_row(q, k, v, dtype, (size_t)p * Sq * Dk, pkv * Skv * Dk, pkv * Skv * Dv, i,
+                          Skv - Sq, Skv, Dk, Dv, scale, causal, Lb, query_padding,
+                          out + ((size_t)p * Sq + i) * Dv, w_row, s_row, NULL);
         }
         free(s_row);
     }
@@ -235,8 +245,9 @@ int oracle_attention_rows_gqa(const void *q, const void *k, const void *v, int d
         size_t pkv = (size_t)b * Hkv + h / G;
         int Lb = sequence_length(kv_len, b, Skv);
         double *s_row = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
-        attention_row(q, k, v, dtype, p * Sq * Dk, pkv * Skv * Dk, pkv * Skv * Dv, i, Sq, Skv, Dk,
-                      Dv, scale, causal, Lb, query_padding, out + (size_t)r * Dv, NULL, s_row);
+        attention_row(q, k, v, dtype, p * Sq * Dk, pkv * Skv * Dk, pkv * Skv * Dv, i, Skv - Sq, Skv,
+                      Dk, Dv, scale, causal, Lb, query_padding, out + (size_t)r * Dv, NULL, s_row,
+                      NULL);
         free(s_row);
     }
     return 0;
@@ -249,4 +260,45 @@ int oracle_attention_rows(const void *q, const void *k, const void *v, int dtype
 {
     return oracle_attention_rows_gqa(q, k, v, dtype, out, B, H, H, Sq, Skv, Dk, Dv, scale, causal,
                                      kv_len, query_padding, rows, n_rows, nthreads);
+}
+
+/*
+ * Prefill of a chunk of Sq new queries against a KV cache, with the
+ * log-sum-exp of every row.  Sequence b holds L_b = cache_len[b] valid cache
+ * positions, the last Sq of which are the chunk's own keys (the cache append
+ * of "Scaled dot-product attention with masking", "The full multi-head
+ * computation"); query i sits at absolute position L_b - Sq + i and sees the
+ * keys j <= L_b - Sq + i ("Attention from scratch" (open-llm-engineering),
+ * "KV cache position drift": cache positions and token positions must agree).
+ * A query with a negative position (L_b < Sq: the chunk is longer than the
+ * sequence) sees no key: its row is zero.
+ *
+ * q: (B,H,Sq,Dk)  k: (B,Hkv,Skv,Dk)  v: (B,Hkv,Skv,Dv)  out: (B,H,Sq,Dv) doubles.
+ * lse: (B,H,Sq) doubles or NULL: log(sum_j exp(scale * q_i.k_j)) over the
+ * visible keys, -inf for a row that sees none.  cache_len: host int32[B] or
+ * NULL (every L_b = Skv).  Returns 0, or -1 on a bad argument.
+ */
+int oracle_attention_cache(const void *q, const void *k, const void *v, int dtype, double *out,
+                           double *lse, int B, int H, int Hkv, int Sq, int Skv, int Dk, int Dv,
+                           double scale, const int32_t *cache_len, int nthreads)
+{
+    if (check_dims(B, H, Sq, Skv, Dk, Dv, dtype) || !out || Hkv <= 0 || H % Hkv)
+        return -1;
+    const int G = H / Hkv;
+    long long n_bh = (long long)B * H;
+    long long p;
+    (void)nthreads;
+#pragma omp parallel for schedule(dynamic) num_threads(nthreads > 0 ? nthreads : 1)
+    for (p = 0; p < n_bh; p++) {
+        int b = (int)(p / H), h = (int)(p % H);
+        size_t pkv = (size_t)b * Hkv + h / G;
+        int Lb = sequence_length(cache_len, b, Skv);
+        double *s_row = (double *)malloc(sizeof(double) * (Skv > 0 ? Skv : 1));
+        for (int i = 0; i < Sq; i++)
+            attention_row(q, k, v, dtype, (size_t)p * Sq * Dk, pkv * Skv * Dk, pkv * Skv * Dv, i,
+                          Lb - Sq, Skv, Dk, Dv, scale, 1, Lb, 0, out + ((size_t)p * Sq + i) * Dv,
+                          NULL, s_row, lse ? lse + (size_t)p * Sq + i : NULL);
+        free(s_row);
+    }
+    return 0;
 }

@@ -312,6 +312,48 @@ def pin_grouped_query_matches_library(att):
                     np.testing.assert_allclose(out[b, :, i], ref[b, :, i], rtol=0, atol=1e-12)
 
 
+def pin_cache_chunk_is_tail_of_full_causal(att):
+    """A chunk of the last Sq tokens of a sequence, run against its KV cache of
+    L_b positions, equals rows L_b - Sq .. L_b - 1 of causal self-attention
+    over those L_b tokens ('Scaled dot-product attention with masking', the
+    cache append before causal attention; 'Attention from scratch'
+    (open-llm-engineering), "KV cache position drift": positions are
+    absolute).  Per-sequence lengths shorter than the cache, grouped heads."""
+    B, H, Hkv, Skv, Sq, D = 3, 4, 2, 9, 3, 5
+    lens = [9, 6, 3]
+    qfull = _rand((B, H, Skv, D), 110)
+    k, v = _rand((B, Hkv, Skv, D), 111), _rand((B, Hkv, Skv, D), 112)
+    q = np.stack([qfull[b, :, L - Sq:L] for b, L in enumerate(lens)])
+    out = att(q, k, v, causal=True, cache_len=np.array(lens, np.int32))
+    for b, L in enumerate(lens):
+        full = att(qfull[b:b + 1, :, :L], k[b:b + 1, :, :L], v[b:b + 1, :, :L], causal=True)
+        np.testing.assert_allclose(out[b], full[0, :, L - Sq:L], rtol=0, atol=1e-13)
+
+
+def pin_lse_is_log_sum_exp(att):
+    """The log-sum-exp output is log(sum_j exp(scale * q_i.k_j)) over exactly
+    the visible keys, computed here by brute force with numpy's logaddexp;
+    -inf for a query whose position precedes the sequence (cache_len < Sq)."""
+    B, H, Hkv, Skv, Sq, D = 2, 4, 1, 7, 4, 3
+    lens = [7, 2]
+    q, k = _rand((B, H, Sq, D), 120), _rand((B, Hkv, Skv, D), 121)
+    v = _rand((B, Hkv, Skv, D), 122)
+    scale = 0.7
+    _, lse = att(q, k, v, scale=scale, causal=True, cache_len=np.array(lens, np.int32), need_lse=True)
+    G = H // Hkv
+    for b, L in enumerate(lens):
+        for h in range(H):
+            for i in range(Sq):
+                vis = [j for j in range(L) if j <= L - Sq + i]
+                s = [scale * float(np.dot(q[b, h, i].astype(np.float64), k[b, h // G, j].astype(np.float64)))
+                     for j in vis]
+                want = np.logaddexp.reduce(s) if s else -np.inf
+                if s:
+                    assert abs(lse[b, h, i] - want) <= 1e-12, (b, h, i, lse[b, h, i], want)
+                else:
+                    assert lse[b, h, i] == -np.inf
+
+
 ALL_PINS = [
     pin_tiny_example_causal,
     pin_kube_dojo_example,
@@ -328,4 +370,6 @@ ALL_PINS = [
     pin_chunk_against_cache,
     pin_key_padding_is_truncation,
     pin_grouped_query_matches_library,
+    pin_cache_chunk_is_tail_of_full_causal,
+    pin_lse_is_log_sum_exp,
 ]

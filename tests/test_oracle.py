@@ -72,21 +72,23 @@ def test_rejects_bad_arguments():
 # Planted mistakes: each replaces one fragment of oracle.c in a private copy.
 # Every mutant stays inside its arrays; each must fail at least one pin.
 MUTANTS = {
-    "mask_polarity_flipped": ("if (causal && j > i + (Skv - Sq))", "if (causal && j < i + (Skv - Sq))"),
-    "causal_diagonal_excluded": ("if (causal && j > i + (Skv - Sq))", "if (causal && j >= i + (Skv - Sq))"),
+    "mask_polarity_flipped": ("if (causal && j > i + off)", "if (causal && j < i + off)"),
+    "causal_diagonal_excluded": ("if (causal && j > i + off)", "if (causal && j >= i + off)"),
     "scale_dropped": ("s_row[j] = scale * dot;", "s_row[j] = dot;"),
     "max_not_subtracted": ("exp(s_row[j] - m)", "exp(s_row[j])"),
     "not_normalised": ("double w = exp(s_row[j] - m) / z;", "double w = exp(s_row[j] - m);"),
-    "padding_off_by_one": ("if (j >= Lb)", "if (j > Lb && j < Skv)"),
+    "padding_off_by_one": ("if (j >= Lb)\n        return 0;", "if (j > Lb)\n        return 0;"),
     "value_rows_reversed": ("v_bh + (size_t)j * Dv + d", "v_bh + (size_t)(Skv - 1 - j) * Dv + d"),
     "dot_drops_last_term": ("for (d = 0; d < Dk; d++)\n            dot +=",
                             "for (d = 0; d < Dk - 1; d++)\n            dot +="),
     "padded_queries_kept": ("if (query_padding && i >= Lb)\n        return;",
                             "if (query_padding && i >= Lb && 0)\n        return;"),
+    "lse_without_max": ("*lse = m + log(z);", "*lse = log(z);"),
+    "cache_offset_from_capacity": ("Lb - Sq, Skv, Dk, Dv, scale, 1, Lb, 0,", "Skv - Sq, Skv, Dk, Dv, scale, 1, Lb, 0,"),
     "kv_head_by_modulo": ("size_t pkv = (size_t)b * Hkv + h / G;", "size_t pkv = (size_t)b * Hkv + h % Hkv;"),
     "keys_from_query_row": ("load_elem(k, dtype, k_bh + (size_t)j * Dk + d)",
-                            "load_elem(k, dtype, k_bh + (size_t)(j < Sq ? j : 0) * Dk + d) * 0.0 + "
-                            "load_elem(q, dtype, q_bh + (size_t)(j < Sq ? j : 0) * Dk + d)"),
+                            "load_elem(k, dtype, k_bh + (size_t)j * Dk + d) * 0.0 + "
+                            "load_elem(q, dtype, q_bh + (size_t)i * Dk + d)"),
 }
 
 
