@@ -121,6 +121,39 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
                           const int32_t *kv_len, int dtype, void *stream);
 
 /*
+ * attn_fwd_chunked -- prefill of a chunk of new queries against a KV cache,
+ * with the log-sum-exp of every row.
+ *
+ * Defines: the cache append before causal attention of "Scaled
+ * dot-product attention with masking" ("The full multi-head computation":
+ * past keys and values are concatenated with the new ones), with positions
+ * kept absolute ("Attention from scratch" (open-llm-engineering), "KV cache
+ * position drift").  Sequence b holds L_b = cache_len[b] valid cache
+ * positions, the last Sq of which are the chunk's own keys and values
+ * (appended by the caller); query i sits at position L_b - Sq + i and sees
+ * keys j <= L_b - Sq + i.  A query whose position is negative (L_b < Sq)
+ * sees no key: its row is zero.  Grouped-query heads as in attn_fwd_gqa.
+ *
+ *   q          (B, H,    Sq,  D)  the chunk's queries
+ *   kcache     (B, H_kv, Skv, D)  cache capacity Skv >= Sq
+ *   vcache     (B, H_kv, Skv, D)
+ *   out        (B, H,    Sq,  D)  written; must not overlap the inputs
+ *   lse        NULL, or device float (B, H, Sq), written: log(sum_j
+ *              exp(scale * q_i . k_j)) over the visible keys (natural log,
+ *              fp32), -inf for a row that sees none.  Not on the pages: it is
+ *              what lets a caller merge attention over split key sets exactly,
+ *              out = sum_c exp(lse_c - LSE) out_c with LSE = log sum_c exp(lse_c).
+ *   cache_len  NULL (every L_b = Skv) or device int32[B], clamped to [0, Skv].
+ *
+ * dtype, D, scale, sizes and errors as in attn_fwd; Sq > Skv returns
+ * ATTN_EINVAL.  With cache_len NULL and no lse this is attn_fwd_gqa with
+ * causal = 1.
+ */
+ATTN_API int attn_fwd_chunked(const void *q, const void *kcache, const void *vcache, void *out,
+                              float *lse, int B, int H, int H_kv, int Sq, int Skv, int D, float scale,
+                              const int32_t *cache_len, int dtype, void *stream);
+
+/*
  * attn_decode -- one new query per (batch, head) against a KV cache.
  *
  * Defines: "Attention from First Principles", section 6 "Under the hood"

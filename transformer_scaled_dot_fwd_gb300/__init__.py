@@ -33,6 +33,7 @@ _vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "attn_fwd_chunked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
@@ -163,6 +164,42 @@ def attn_fwd(q, k, v, out=None, scale: Optional[float] = None, causal: bool = Fa
                                 _stream_handle(stream))
     _check(rc)
     return out
+
+
+def attn_fwd_chunked(q, kcache, vcache, out=None, lse=None, scale: Optional[float] = None,
+                     cache_len=None, return_lse: bool = False, stream=None):
+    """Prefill of a chunk of (B, H, Sq, D) queries against a (B, H_kv, Skv, D)
+    KV cache whose last positions hold the chunk's own keys/values: query i
+    of sequence b sits at position cache_len[b] - Sq + i (causal).  Returns
+    ``out``, or ``(out, lse)`` with the (B, H, Sq) fp32 log-sum-exp when
+    ``return_lse`` (or an ``lse`` tensor) is given.  See include/attn.h.
+    """
+    for name, t in (("q", q), ("kcache", kcache), ("vcache", vcache)):
+        _check_tensor(name, t, 4)
+    B, H, Sq, D = q.shape
+    H_kv, Skv = kcache.shape[1], kcache.shape[2]
+    if (tuple(kcache.shape) != (B, H_kv, Skv, D) or tuple(vcache.shape) != (B, H_kv, Skv, D)
+            or H % H_kv):
+        raise ValueError("kcache and vcache must be (B, H_kv, Skv, D) matching q, with H_kv dividing H")
+    if not (q.dtype == kcache.dtype == vcache.dtype):
+        raise TypeError("q, kcache, vcache must share one dtype")
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(q)
+    _check_tensor("out", out, 4)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_tensor("lse", lse, 3)
+        if tuple(lse.shape) != (B, H, Sq) or lse.dtype != torch.float32:
+            raise ValueError("lse must be a float32 (B, H, Sq) tensor")
+    cl = _kv_len_arg(cache_len, B, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().attn_fwd_chunked(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(out), _ptr(lse), B, H, H_kv,
+                                Sq, Skv, D, float(scale), _ptr(cl), _dtype_code(q), _stream_handle(stream))
+    _check(rc)
+    return (out, lse) if lse is not None else out
 
 
 def attn_decode(q, kcache, vcache, out=None, kv_len=None, stream=None):

@@ -191,9 +191,11 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, in
     return attn_fwd_gqa(q, k, v, out, B, H, H, Sq, Skv, D, scale, causal, kv_len, dtype, stream);
 }
 
-ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out, int B, int H,
-                          int H_kv, int Sq, int Skv, int D, float scale, int causal,
-                          const int32_t *kv_len, int dtype, void *stream) {
+// Shared by attn_fwd_gqa (chunked = 0, no lse) and attn_fwd_chunked (causal,
+// kv_len = cache lengths, chunked = 1, optional lse).
+static int fwd_impl(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H,
+                    int H_kv, int Sq, int Skv, int D, float scale, int causal, const int32_t *kv_len,
+                    int chunked, int dtype, void *stream) {
     g_last_error[0] = '\0';
     if (B < 1 || H < 1 || Sq < 0 || Skv < 0)
         return fail(ATTN_EINVAL, "attn_fwd: need B >= 1, H >= 1, Sq >= 0, Skv >= 0 (got %d, %d, %d, %d)", B, H, Sq, Skv);
@@ -207,7 +209,10 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
     if (!(scale >= 0.f) || isinf(scale)) return fail(ATTN_EINVAL, "attn_fwd: scale must be finite and >= 0");
     if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_fwd: causal must be 0 or 1");
     if (causal && Sq > Skv) return fail(ATTN_EINVAL, "attn_fwd: causal needs Sq <= Skv (got %d > %d)", Sq, Skv);
-    if (kv_len && Sq != Skv) return fail(ATTN_EINVAL, "attn_fwd: kv_len needs Sq == Skv (self-attention)");
+    if (kv_len && !chunked && Sq != Skv)
+        return fail(ATTN_EINVAL, "attn_fwd: kv_len needs Sq == Skv (self-attention)");
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(ATTN_EINVAL, "attn_fwd: lse must be 4-byte aligned");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
         return fail(ATTN_EINVAL, "attn_fwd: q, k, v and out must be 16-byte aligned");
     if (kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u))
@@ -223,6 +228,10 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
     if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||
         overlaps(out, q_bytes, v, kv_bytes))
         return fail(ATTN_EINVAL, "attn_fwd: out overlaps an input");
+    const size_t lse_bytes = static_cast<size_t>(bh) * Sq * sizeof(float);
+    if (lse && (overlaps(lse, lse_bytes, q, q_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+                overlaps(lse, lse_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, out, q_bytes)))
+        return fail(ATTN_EINVAL, "attn_fwd: lse overlaps another tensor");
     if (Sq == 0) return ATTN_OK;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -233,7 +242,8 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
     int *status = nullptr;
     int rc = status_word(&status);
     if (rc) return rc;
-    FwdArgs a{q, k, v, out, kv_len, B, H, Sq, Skv, D, scale, causal, status, st, num_sms(), H_kv};
+    FwdArgs a{q, k, v, out, kv_len, B, H, Sq, Skv, D, scale, causal, status, st, num_sms(), H_kv,
+              chunked, lse};
     cudaError_t e;
     if (dtype == ATTN_F32) {
         if (B > 65535 || H > 65535) return fail(ATTN_EINVAL, "attn_fwd: B and H must be <= 65535 for fp32");
@@ -246,6 +256,20 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
         e = launch_prefill_tc(a, tq, tk, tv);
     }
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd launch");
+}
+
+ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out, int B, int H,
+                          int H_kv, int Sq, int Skv, int D, float scale, int causal,
+                          const int32_t *kv_len, int dtype, void *stream) {
+    return fwd_impl(q, k, v, out, nullptr, B, H, H_kv, Sq, Skv, D, scale, causal, kv_len, 0, dtype,
+                    stream);
+}
+
+ATTN_API int attn_fwd_chunked(const void *q, const void *kcache, const void *vcache, void *out,
+                              float *lse, int B, int H, int H_kv, int Sq, int Skv, int D, float scale,
+                              const int32_t *cache_len, int dtype, void *stream) {
+    return fwd_impl(q, kcache, vcache, out, lse, B, H, H_kv, Sq, Skv, D, scale, 1, cache_len, 1, dtype,
+                    stream);
 }
 
 ATTN_API int attn_decode_splits(int B, int H, int Skv, int D) {

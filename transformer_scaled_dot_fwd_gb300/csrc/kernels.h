@@ -19,6 +19,11 @@ struct FwdArgs {
     cudaStream_t stream;
     int n_sm;               // streaming multiprocessors on the device
     int H_kv;               // key/value heads (divides H); query head h reads head h / (H / H_kv)
+    // Chunk-against-cache mode (attn_fwd_chunked): kv_len[b] is the cached
+    // length L_b, query i sits at position L_b - Sq + i (causal), and no query
+    // row is treated as padding.
+    int chunked;
+    float *lse;             // (B, H, Sq) natural-log log-sum-exp of each row, or nullptr
 };
 
 struct DecodeArgs {

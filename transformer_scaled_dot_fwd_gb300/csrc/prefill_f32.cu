@@ -44,8 +44,9 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
 
     int L = a.Skv;
     if (a.kv_len) L = min(max(a.kv_len[b], 0), a.Skv);
-    const int off = a.Skv - a.Sq;  // causal: key j visible from query i iff j <= i + off
-    const bool row_valid = i < a.Sq && !(a.kv_len && i >= L);
+    // causal: key j visible from query i iff j <= i + off
+    const int off = a.chunked ? L - a.Sq : a.Skv - a.Sq;
+    const bool row_valid = i < a.Sq && !(!a.chunked && a.kv_len && i >= L);
     int lim = L;                   // keys [0, lim) are visible from row i
     if (a.causal) lim = min(lim, i + off + 1);
     if (!row_valid) lim = 0;
@@ -105,9 +106,12 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
     }
 
     if (i < a.Sq) {
-        const float inv = (row_valid && l > 0.f) ? 1.f / l : 0.f;
+        const bool seen = row_valid && l > 0.f;
+        const float inv = seen ? 1.f / l : 0.f;
 #pragma unroll
         for (int d = 0; d < DL; ++d) O[static_cast<size_t>(i) * D + d * kLanesPerRow + t] = o[d] * inv;
+        // log(sum_j exp(scale * s_j)) = ln 2 * (m + log2 l), m and l in log2 units
+        if (a.lse && t == 0) a.lse[bh * a.Sq + i] = seen ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
 }
 

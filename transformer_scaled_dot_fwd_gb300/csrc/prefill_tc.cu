@@ -91,6 +91,7 @@ struct Item {
     int row_base, row_step, bh_base, bh_step;
     int bh_kv;          // b * H_kv + h / G: the key/value head both tiles read
     int Lb;
+    int off;            // causal: key j visible from query row i iff j <= i + off
     int n_kv[kQTiles];  // K/V tiles each query tile needs (0: tile empty or fully padded)
     int N;              // max of n_kv
 };
@@ -197,17 +198,20 @@ __device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_major
     it.bh_kv = b * a.H_kv + h0 / G;
     it.Lb = a.Skv;
     if (a.kv_len) it.Lb = min(max(a.kv_len[b], 0), a.Skv);
-    const int off = a.Skv - a.Sq;  // causal: key j visible from query i iff j <= i + off
+    // Chunk against a cache: the Sq queries are the last Sq positions of the
+    // sequence's L_b; otherwise the last query is aligned with the last key.
+    it.off = a.chunked ? it.Lb - a.Sq : a.Skv - a.Sq;
+    const bool query_padding = a.kv_len && !a.chunked;  // rows i >= L_b of a padded batch
     it.N = 0;
 #pragma unroll
     for (int x = 0; x < kQTiles; ++x) {
         const int row0 = it.row_base + x * it.row_step;
         int n = 0;
-        if (row0 < a.Sq && !(a.kv_len && row0 >= it.Lb)) {
+        if (row0 < a.Sq && !(query_padding && row0 >= it.Lb)) {
             int last = min(a.Sq - 1, row0 + kBM - 1);
-            if (a.kv_len) last = min(last, it.Lb - 1);
-            const int hi = a.causal ? min(it.Lb, last + off + 1) : it.Lb;
-            n = (hi + kBN - 1) / kBN;
+            if (query_padding) last = min(last, it.Lb - 1);
+            const int hi = a.causal ? min(it.Lb, last + it.off + 1) : it.Lb;
+            n = (max(hi, 0) + kBN - 1) / kBN;
         }
         it.n_kv[x] = n;
         it.N = max(it.N, n);
@@ -225,6 +229,7 @@ __device__ __forceinline__ void publish_item(Bars &bars, int slot, const Item &i
     d.bh_step = it.bh_step;
     d.bh_kv = it.bh_kv;
     d.Lb = it.Lb;
+    d.off = it.off;
     d.n_kv[0] = it.n_kv[0];
     d.n_kv[1] = it.n_kv[1];
     d.N = it.N;
@@ -238,6 +243,7 @@ __device__ __forceinline__ Item read_item(Bars &bars, int k) {
     it.bh_step = sv.bh_step;
     it.bh_kv = sv.bh_kv;
     it.Lb = sv.Lb;
+    it.off = sv.off;
     it.n_kv[0] = sv.n_kv[0];
     it.n_kv[1] = sv.n_kv[1];
     it.N = sv.N;
@@ -321,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t < n_items) {
                     it = decode_item(t, a, n_major);
                 } else {
-                    it = Item{0, 0, 0, 0, 0, 0, {0, 0}, -1};
+                    it = Item{0, 0, 0, 0, 0, 0, 0, {0, 0}, -1};
                 }
                 publish_item(bars, slot, it);
                 mbar_arrive(&bars.item_full[slot]);
@@ -497,7 +503,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_s = t_lane + L::s_col(x);
         const uint32_t t_o = t_lane + L::o_col(x);
         const float sl2 = a.scale * kLog2e;
-        const int off = a.Skv - a.Sq;
         const uint32_t stage = smem_u32(smem + L::kStageOff + (warp - 4) * L::kStageBytes);
         uint32_t sp = 0, o_uses = 0;
         bool ok = true;
@@ -513,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int i = it.row_base + x * it.row_step + r;  // query row
                 n = x ? it.n_kv[1] : it.n_kv[0];  // a select: x is not a compile-time index here
-                lim = a.causal ? min(it.Lb, i + off + 1) : it.Lb;  // keys [0, lim) visible
+                lim = a.causal ? min(it.Lb, i + it.off + 1) : it.Lb;  // keys [0, lim) visible
             }
             float m_run = -INFINITY, l = 0.f;
 
@@ -665,12 +670,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (n > 0) ++o_uses;
             // the item again, from its ring slot (nothing of it stays live through the tile loop)
-            const Item it = read_item(bars, k);  // again: nothing of it stayed live through the tiles
+            const Item it = read_item(bars, k);
             release_item(bars, k);
             const int row0 = it.row_base + x * it.row_step;
             const int i = row0 + r;
-            const bool zero_row = !have_o || (a.kv_len && i >= it.Lb) || !(l > 0.f);
+            const bool zero_row = !have_o || (a.kv_len && !a.chunked && i >= it.Lb) || !(l > 0.f);
             const float inv = zero_row ? 0.f : 1.f / l;
+            // log(sum_j exp(scale * s_j)) = ln 2 * (m_run + log2 l): l is kept relative to
+            // m_run whether or not the lazy rescale has moved it
+            if (a.lse && i < a.Sq)
+                a.lse[static_cast<size_t>(it.bh_base + x * it.bh_step) * a.Sq + i] =
+                    zero_row ? -INFINITY : (m_run + log2f(l)) * 0.6931471805599453f;
             __nv_bfloat16 *obh = static_cast<__nv_bfloat16 *>(a.out) + static_cast<size_t>(it.bh_base + x * it.bh_step) * a.Sq * D;
             const int wrow0 = row0 + quarter * 32;  // first row of this warp
 #pragma unroll
