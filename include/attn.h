@@ -84,9 +84,14 @@ extern "C" {
  *           pages' choice, "Why divide by the square root of the head
  *           dimension?")
  *   causal  0 or 1; causal with Sq > Skv is rejected (ATTN_EINVAL)
- *   kv_len  NULL, or device int32[B]: per-sequence valid length.  With
- *           kv_len the call is self-attention over a right-padded batch and
- *           needs Sq == Skv; query rows i >= kv_len[b] output zeros.
+ *   kv_len  NULL, or device int32[B]: per-sequence valid length; keys
+ *           j >= kv_len[b] are masked.  With Sq == Skv the call is
+ *           self-attention over a right-padded batch and query rows
+ *           i >= kv_len[b] output zeros too.  With Sq != Skv only non-causal
+ *           calls take kv_len (cross-attention with a padded source,
+ *           "Attention from Scratch" (kube-dojo), Part 7: the padding mask
+ *           spans the source length); for a causal chunk of queries against a
+ *           cache use attn_fwd_chunked.
  *   dtype   ATTN_BF16: D must be 64 or 128.  ATTN_F32: D must be 64 or 128.
  *
  * Sizes: B, H >= 1; Sq, Skv >= 0 (an empty call returns ATTN_OK and does
@@ -152,6 +157,28 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
 ATTN_API int attn_fwd_chunked(const void *q, const void *kcache, const void *vcache, void *out,
                               float *lse, int B, int H, int H_kv, int Sq, int Skv, int D, float scale,
                               const int32_t *cache_len, int dtype, void *stream);
+
+/*
+ * attn_fwd_debug -- the general attention of "Attention from Scratch"
+ * (kube-dojo), Part 2, for inspection: T_q != T_k, value depth d_v != d_k,
+ * and the attention weights returned with the output (Part 4 "Attention
+ * Maps").  One warp per query row in fp32; not a fast path.
+ *
+ *   q        (B, H,    Sq,  Dk)     dtype ATTN_F32 or ATTN_BF16
+ *   k        (B, H_kv, Skv, Dk)
+ *   v        (B, H_kv, Skv, Dv)
+ *   out      (B, H,    Sq,  Dv)     written, in the input dtype
+ *   weights  NULL or device float (B, H, Sq, Skv), written: the softmax
+ *            weights of each row, exactly 0 for a masked key, all 0 for a
+ *            row that sees no key (and for a padded query row)
+ *
+ * Dk, Dv in [1, 256]; Skv <= 16384 (ATTN_EUNSUPPORTED above); tensors
+ * aligned to their element size.  scale, causal, kv_len, H_kv and the mask
+ * rules are those of attn_fwd / attn_fwd_gqa.
+ */
+ATTN_API int attn_fwd_debug(const void *q, const void *k, const void *v, void *out, float *weights,
+                            int B, int H, int H_kv, int Sq, int Skv, int Dk, int Dv, float scale,
+                            int causal, const int32_t *kv_len, int dtype, void *stream);
 
 /*
  * attn_decode -- one new query per (batch, head) against a KV cache.

@@ -67,7 +67,7 @@ def fwd(lib, q=Q, k=K, v=V, o=O, B=2, H=2, Sq=16, Skv=16, D=128, scale=0.125, ca
     (dict(scale=-1.0), attn.ATTN_EINVAL),
     (dict(causal=2), attn.ATTN_EINVAL),
     (dict(Sq=17, Skv=16), attn.ATTN_EINVAL),                 # causal with Sq > Skv
-    (dict(causal=0, Sq=8, kl=KL), attn.ATTN_EINVAL),         # kv_len needs Sq == Skv
+    (dict(causal=1, Sq=8, kl=KL), attn.ATTN_EINVAL),         # causal kv_len needs Sq == Skv
     (dict(q=ctypes.c_void_p(0x10000008)), attn.ATTN_EINVAL),  # misaligned
     (dict(kl=ctypes.c_void_p(0x50000002)), attn.ATTN_EINVAL),
     (dict(o=ctypes.c_void_p(0x10000000 + 4096)), attn.ATTN_EINVAL),  # out overlaps q
@@ -137,3 +137,32 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b|liboracle|oracle\.c", text, re.M), \
                     f"{f} loads the oracle"
+
+
+def test_new_entry_points_reject_bad_arguments(attn_lib):
+    """Grouped-query, chunked and debug entry points validate on the host
+    before any CUDA call (fake pointers are never dereferenced)."""
+    f, i = ctypes.c_float, attn.ATTN_EINVAL
+    # attn_fwd_gqa: H_kv must divide H
+    assert attn_lib.attn_fwd_gqa(Q, K, V, O, 2, 6, 4, 16, 16, 128, f(0.1), 1, None, attn.ATTN_BF16, None) == i
+    assert attn_lib.attn_fwd_gqa(Q, K, V, O, 2, 6, 0, 16, 16, 128, f(0.1), 1, None, attn.ATTN_BF16, None) == i
+    # attn_fwd_chunked: the chunk cannot be longer than the cache
+    assert attn_lib.attn_fwd_chunked(Q, K, V, O, None, 2, 4, 2, 17, 16, 128, f(0.1), None,
+                                     attn.ATTN_BF16, None) == i
+    # attn_fwd_chunked: lse must be 4-byte aligned and must not overlap out
+    assert attn_lib.attn_fwd_chunked(Q, K, V, O, ctypes.c_void_p(0x60000002), 2, 4, 2, 8, 16, 128, f(0.1),
+                                     None, attn.ATTN_BF16, None) == i
+    assert attn_lib.attn_fwd_chunked(Q, K, V, O, O, 2, 4, 2, 8, 16, 128, f(0.1), None,
+                                     attn.ATTN_BF16, None) == i
+    # attn_fwd_debug: head depths and key count bounds
+    assert attn_lib.attn_fwd_debug(Q, K, V, O, None, 1, 2, 2, 4, 7, 257, 2, f(0.5), 0, None,
+                                   attn.ATTN_F32, None) == i
+    assert attn_lib.attn_fwd_debug(Q, K, V, O, None, 1, 2, 2, 4, 7, 4, 0, f(0.5), 0, None,
+                                   attn.ATTN_F32, None) == i
+    assert attn_lib.attn_fwd_debug(Q, K, V, O, None, 1, 2, 2, 4, 16385, 4, 2, f(0.5), 0, None,
+                                   attn.ATTN_F32, None) == attn.ATTN_EUNSUPPORTED
+    assert attn_lib.attn_fwd_debug(Q, K, V, O, None, 1, 2, 2, 8, 4, 4, 2, f(0.5), 1, None,
+                                   attn.ATTN_F32, None) == i  # causal with Sq > Skv
+    # attn_decode_gqa: H_kv must divide H
+    assert attn_lib.attn_decode_gqa(Q, K, V, O, 2, 8, 3, 64, 128, None, attn.ATTN_BF16, None) == i
+    assert attn.attn_last_error() != ""

@@ -34,6 +34,7 @@ SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_chunked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
+    "attn_fwd_debug": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
@@ -200,6 +201,37 @@ def attn_fwd_chunked(q, kcache, vcache, out=None, lse=None, scale: Optional[floa
                                 Sq, Skv, D, float(scale), _ptr(cl), _dtype_code(q), _stream_handle(stream))
     _check(rc)
     return (out, lse) if lse is not None else out
+
+
+def attn_fwd_debug(q, k, v, out=None, weights=None, scale: Optional[float] = None, causal: bool = False,
+                   kv_len=None, return_weights: bool = False, stream=None):
+    """General attention for inspection: q (B, H, Sq, Dk), k (B, H_kv, Skv, Dk),
+    v (B, H_kv, Skv, Dv); returns out (B, H, Sq, Dv), or (out, weights) with
+    the (B, H, Sq, Skv) fp32 attention weights.  See include/attn.h."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, 4)
+    B, H, Sq, Dk = q.shape
+    H_kv, Skv, Dv = k.shape[1], k.shape[2], v.shape[3]
+    if tuple(k.shape) != (B, H_kv, Skv, Dk) or tuple(v.shape[:3]) != (B, H_kv, Skv) or H % H_kv:
+        raise ValueError("k must be (B, H_kv, Skv, Dk) and v (B, H_kv, Skv, Dv), with H_kv dividing H")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    torch = _torch()
+    if out is None:
+        out = torch.empty((B, H, Sq, Dv), dtype=q.dtype, device=q.device)
+    _check_tensor("out", out, 4)
+    if weights is None and return_weights:
+        weights = torch.empty((B, H, Sq, Skv), dtype=torch.float32, device=q.device)
+    if weights is not None:
+        _check_tensor("weights", weights, 4)
+    kl = _kv_len_arg(kv_len, B, q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(Dk)
+    rc = lib().attn_fwd_debug(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(weights), B, H, H_kv, Sq, Skv,
+                              Dk, Dv, float(scale), int(bool(causal)), _ptr(kl), _dtype_code(q),
+                              _stream_handle(stream))
+    _check(rc)
+    return (out, weights) if weights is not None else out
 
 
 def attn_decode(q, kcache, vcache, out=None, kv_len=None, stream=None):

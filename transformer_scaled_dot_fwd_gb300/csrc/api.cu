@@ -209,8 +209,8 @@ static int fwd_impl(const void *q, const void *k, const void *v, void *out, floa
     if (!(scale >= 0.f) || isinf(scale)) return fail(ATTN_EINVAL, "attn_fwd: scale must be finite and >= 0");
     if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_fwd: causal must be 0 or 1");
     if (causal && Sq > Skv) return fail(ATTN_EINVAL, "attn_fwd: causal needs Sq <= Skv (got %d > %d)", Sq, Skv);
-    if (kv_len && !chunked && Sq != Skv)
-        return fail(ATTN_EINVAL, "attn_fwd: kv_len needs Sq == Skv (self-attention)");
+    if (kv_len && !chunked && causal && Sq != Skv)
+        return fail(ATTN_EINVAL, "attn_fwd: causal kv_len needs Sq == Skv (a chunk against a cache is attn_fwd_chunked)");
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
         return fail(ATTN_EINVAL, "attn_fwd: lse must be 4-byte aligned");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
@@ -270,6 +270,49 @@ ATTN_API int attn_fwd_chunked(const void *q, const void *kcache, const void *vca
                               const int32_t *cache_len, int dtype, void *stream) {
     return fwd_impl(q, kcache, vcache, out, lse, B, H, H_kv, Sq, Skv, D, scale, 1, cache_len, 1, dtype,
                     stream);
+}
+
+ATTN_API int attn_fwd_debug(const void *q, const void *k, const void *v, void *out, float *weights,
+                            int B, int H, int H_kv, int Sq, int Skv, int Dk, int Dv, float scale,
+                            int causal, const int32_t *kv_len, int dtype, void *stream) {
+    g_last_error[0] = '\0';
+    if (B < 1 || H < 1 || Sq < 0 || Skv < 0)
+        return fail(ATTN_EINVAL, "attn_fwd_debug: need B >= 1, H >= 1, Sq >= 0, Skv >= 0");
+    if (H_kv < 1 || H % H_kv != 0)
+        return fail(ATTN_EINVAL, "attn_fwd_debug: H_kv must divide H (got H = %d, H_kv = %d)", H, H_kv);
+    if (Dk < 1 || Dk > 256 || Dv < 1 || Dv > 256)
+        return fail(ATTN_EINVAL, "attn_fwd_debug: Dk and Dv must be in [1, 256] (got %d, %d)", Dk, Dv);
+    if (Skv > 16384) return fail(ATTN_EUNSUPPORTED, "attn_fwd_debug: Skv = %d above 16384", Skv);
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return fail(ATTN_EINVAL, "attn_fwd_debug: unknown dtype %d", dtype);
+    if (!(scale >= 0.f) || isinf(scale)) return fail(ATTN_EINVAL, "attn_fwd_debug: scale must be finite and >= 0");
+    if (causal != 0 && causal != 1) return fail(ATTN_EINVAL, "attn_fwd_debug: causal must be 0 or 1");
+    if (causal && Sq > Skv) return fail(ATTN_EINVAL, "attn_fwd_debug: causal needs Sq <= Skv (got %d > %d)", Sq, Skv);
+    if (kv_len && causal && Sq != Skv)
+        return fail(ATTN_EINVAL, "attn_fwd_debug: causal kv_len needs Sq == Skv");
+    if ((Sq > 0 && (!q || !out)) || (Skv > 0 && (!k || !v)))
+        return fail(ATTN_EINVAL, "attn_fwd_debug: q and out (Sq > 0), k and v (Skv > 0) must not be NULL");
+    const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
+    const uintptr_t amask = esz - 1;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+         reinterpret_cast<uintptr_t>(out)) & amask)
+        return fail(ATTN_EINVAL, "attn_fwd_debug: tensors must be aligned to their element size");
+    if ((kv_len && (reinterpret_cast<uintptr_t>(kv_len) & 3u)) || (weights && (reinterpret_cast<uintptr_t>(weights) & 3u)))
+        return fail(ATTN_EINVAL, "attn_fwd_debug: kv_len and weights must be 4-byte aligned");
+    const long long rows = static_cast<long long>(B) * H * Sq;
+    if (rows >= (1LL << 31)) return fail(ATTN_EINVAL, "attn_fwd_debug: B*H*Sq is too large");
+    const long long bh_kv = static_cast<long long>(B) * H_kv;
+    const size_t q_bytes = static_cast<size_t>(rows) * Dk * esz, o_bytes = static_cast<size_t>(rows) * Dv * esz;
+    const size_t k_bytes = static_cast<size_t>(bh_kv) * Skv * Dk * esz, v_bytes = static_cast<size_t>(bh_kv) * Skv * Dv * esz;
+    const size_t w_bytes = static_cast<size_t>(rows) * Skv * sizeof(float);
+    if (overlaps(out, o_bytes, q, q_bytes) || overlaps(out, o_bytes, k, k_bytes) || overlaps(out, o_bytes, v, v_bytes) ||
+        (weights && (overlaps(weights, w_bytes, q, q_bytes) || overlaps(weights, w_bytes, k, k_bytes) ||
+                     overlaps(weights, w_bytes, v, v_bytes) || overlaps(weights, w_bytes, out, o_bytes))))
+        return fail(ATTN_EINVAL, "attn_fwd_debug: out or weights overlaps another tensor");
+    if (rows == 0) return ATTN_OK;
+    DebugArgs a{q, k, v, out, weights, kv_len, B, H, H_kv, Sq, Skv, Dk, Dv, scale, causal,
+                dtype == ATTN_BF16 ? 1 : 0, static_cast<cudaStream_t>(stream)};
+    const cudaError_t e = launch_debug_attention(a);
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd_debug launch");
 }
 
 ATTN_API int attn_decode_splits(int B, int H, int Skv, int D) {

@@ -45,6 +45,20 @@ struct DecodeArgs {
 constexpr int kDecodeMaxChunk = 1024;
 constexpr int kDecodeGqaMaxChunk = 512;
 
+// Debug attention (attn_fwd_debug): any d_k, d_v <= 256, optional weights.
+struct DebugArgs {
+    const void *q, *k, *v;  // (B, H, Sq, Dk), (B, H_kv, Skv, Dk), (B, H_kv, Skv, Dv)
+    void *out;              // (B, H, Sq, Dv), input dtype
+    float *weights;         // (B, H, Sq, Skv) fp32 or nullptr
+    const int32_t *kv_len;  // device int32[B] or nullptr
+    int B, H, H_kv, Sq, Skv, Dk, Dv;
+    float scale;
+    int causal;
+    int dtype_bf16;
+    cudaStream_t stream;
+};
+cudaError_t launch_debug_attention(const DebugArgs &a);
+
 // fp32 SIMT prefill (D in {64, 128}).
 cudaError_t launch_prefill_f32(const FwdArgs &a);
 

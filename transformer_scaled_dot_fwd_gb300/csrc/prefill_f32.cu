@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
     if (a.kv_len) L = min(max(a.kv_len[b], 0), a.Skv);
     // causal: key j visible from query i iff j <= i + off
     const int off = a.chunked ? L - a.Sq : a.Skv - a.Sq;
-    const bool row_valid = i < a.Sq && !(!a.chunked && a.kv_len && i >= L);
+    const bool row_valid = i < a.Sq && !(!a.chunked && a.kv_len && a.Sq == a.Skv && i >= L);
     int lim = L;                   // keys [0, lim) are visible from row i
     if (a.causal) lim = min(lim, i + off + 1);
     if (!row_valid) lim = 0;

@@ -201,7 +201,9 @@ __device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_major
     // Chunk against a cache: the Sq queries are the last Sq positions of the
     // sequence's L_b; otherwise the last query is aligned with the last key.
     it.off = a.chunked ? it.Lb - a.Sq : a.Skv - a.Sq;
-    const bool query_padding = a.kv_len && !a.chunked;  // rows i >= L_b of a padded batch
+    // rows i >= L_b of a right-padded self-attention batch (with Sq != Skv,
+    // non-causal cross-attention, kv_len masks keys only)
+    const bool query_padding = a.kv_len && !a.chunked && a.Sq == a.Skv;
     it.N = 0;
 #pragma unroll
     for (int x = 0; x < kQTiles; ++x) {
@@ -674,7 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             release_item(bars, k);
             const int row0 = it.row_base + x * it.row_step;
             const int i = row0 + r;
-            const bool zero_row = !have_o || (a.kv_len && !a.chunked && i >= it.Lb) || !(l > 0.f);
+            const bool zero_row =
+                !have_o || (a.kv_len && !a.chunked && a.Sq == a.Skv && i >= it.Lb) || !(l > 0.f);
             const float inv = zero_row ? 0.f : 1.f / l;
             // log(sum_j exp(scale * s_j)) = ln 2 * (m_run + log2 l): l is kept relative to
             // m_run whether or not the lazy rescale has moved it
