@@ -327,6 +327,8 @@ def run_ours(args):
         return run_decode_only(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
     if args.only == "decode-gqa":
         return run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
+    if args.only == "s-sweep":
+        return run_s_sweep(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
     q, k, v, kv_len = wl.prefill_inputs(w, device=device, seed=w.seed + 1000 * rank)
     out = torch.empty_like(q)
 
@@ -470,6 +472,79 @@ def run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, ra
     return 0
 
 
+def loglog_slope(xs, ys):
+    """Least-squares slope of log(y) against log(x)."""
+    lx, ly = np.log(np.asarray(xs, float)), np.log(np.asarray(ys, float))
+    return float(np.polyfit(lx, ly, 1)[0]) if len(xs) >= 2 else None
+
+
+def run_s_sweep(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
+    """Prefill time against sequence length at fixed batch (B4 H32 D128 bf16),
+    causal and not: 'Attention from First Principles', Exercises, D (time vs S
+    on log-log axes, slope 2 for the score work; where a naive implementation
+    runs out of memory), with the score-tensor sizes of its section 5 and
+    'Scaled dot-product attention with masking', "The memory problem".
+
+    For each S: CUDA-event time per call (L2 flushed between calls), TFLOP/s,
+    and the bytes a materialising implementation needs for the (B, H, S, S)
+    bf16 score tensor alone, against the device's memory.  This path holds
+    no score tensor: its device memory is Q, K, V and O.  One JSON line per
+    (S, causal), then a summary line with the log-log slopes; not part of the
+    default run."""
+    sh = wl.S_SWEEP_SHAPE
+    B, H, D = sh["B"], sh["H"], sh["D"]
+    total_mem = torch.cuda.get_device_properties(device).total_memory
+    tflops_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    rows = {True: [], False: []}
+    first_naive_oom = None
+    for S in wl.S_SWEEP:
+        q, k, v = wl.s_sweep_inputs(S, device, rank)
+        out = torch.empty_like(q)
+        qkvo = 4 * q.numel() * q.element_size()
+        naive_scores = B * H * S * S * 2
+        naive_fits = naive_scores + qkvo <= total_mem
+        if not naive_fits and first_naive_oom is None:
+            first_naive_oom = S
+        for causal in (True, False):
+            def step():
+                attn.attn_fwd(q, k, v, out=out, causal=causal)
+
+            flops = prefill_flops(B, H, S, S, D, causal)
+            est_ms = flops / (0.8 * tflops_peak * 1e12) * 1e3 + 0.01
+            steps = int(min(args.steps, max(3, math.ceil(300.0 / est_ms))))
+            for _ in range(args.warmup):
+                step()
+            attn.attn_device_status()
+            ms = time_steps(step, steps, stream, flush)
+            attn.attn_device_status()
+            avg = max_over_ranks(dist, float(sum(ms)), device) / steps
+            rows[causal].append((S, avg))
+            if rank == 0:
+                print(json.dumps({"s_sweep": {
+                    "workload": f"{'causal' if causal else 'non-causal'} prefill B{B} H{H} S{S} D{D} bf16",
+                    "S": S, "causal": causal, "steps": steps, "ms_per_call": avg,
+                    "flops_per_call": flops, "TFLOP_per_s": flops / (avg * 1e-3) / 1e12,
+                    "frac_of_peak": flops / (avg * 1e-3) / 1e12 / tflops_peak,
+                    "device_bytes_qkvo": qkvo, "naive_score_tensor_bytes": naive_scores,
+                    "naive_fits_in_device_memory": bool(naive_fits)}}), flush=True)
+        del q, k, v, out
+        torch.cuda.empty_cache()
+    if rank == 0:
+        summary = {"device_memory_bytes": total_mem, "peak_tflops": tflops_peak, "peak_source": peak_src,
+                   "first_S_where_naive_scores_exceed_memory": first_naive_oom,
+                   "l2": "flushed between calls (256 MB write), outside the timed events"}
+        for causal in (True, False):
+            pts = rows[causal]
+            key = "causal" if causal else "non_causal"
+            summary[f"slope_{key}_all"] = loglog_slope([s for s, _ in pts], [t for _, t in pts])
+            big = [(s, t) for s, t in pts if s >= 2048]
+            summary[f"slope_{key}_S_ge_2048"] = loglog_slope([s for s, _ in big], [t for _, t in big])
+        print(json.dumps({"s_sweep_summary": summary}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_decode_only(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
     decode = decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
     if rank == 0:
@@ -520,8 +595,9 @@ def main():
                     help="approximate CPU time of the fp64 checker baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "decode-gqa"], default="all",
-                    help="profiling runs: time one kernel family only")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "decode-gqa", "s-sweep"],
+                    default="all", help="profiling runs: time one kernel family only; s-sweep times "
+                    "prefill against sequence length")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="profiling runs: smaller decode batch than the workload's 64")
     args = ap.parse_args()

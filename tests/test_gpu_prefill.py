@@ -261,3 +261,26 @@ def test_decode_equals_last_causal_row(gpu):
     attn.attn_device_status()
     diff = (full[:, :, S - 1].float() - dec.float()).abs().max().item()
     assert diff <= 2e-2
+
+
+@pytest.mark.parametrize("S", [128, 65536])
+@pytest.mark.parametrize("causal", [True, False])
+def test_s_sweep_extremes_sampled(gpu, S, causal):
+    """The sequence-length sweep's smallest and largest lengths (B4 H32 D128
+    bf16; at S = 65536 a materialised score tensor would not fit in HBM), in
+    the launch configuration the sweep times.  The oracle evaluates sampled
+    rows of three (b, h) slices, each slice passed alone."""
+    q, k, v = wl.s_sweep_inputs(S, "cuda")
+    out = attn.attn_fwd(q, k, v, causal=causal)
+    attn.attn_device_status()
+    rng = np.random.default_rng(S + causal)
+    B, H = q.shape[0], q.shape[1]
+    for b, h in ((0, 0), (B - 1, H - 1), (1, 17)):
+        pick = sorted(i for i in {0, 1, 127, 128, S // 2, S - 2, S - 1} | set(rng.integers(0, S, size=8).tolist())
+                      if i < S)
+        rows = np.array([(0, 0, i) for i in pick], dtype=np.int64)
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        ref = oracle.attention_rows(q[sl].cpu(), k[sl].cpu(), v[sl].cpu(), rows, causal=causal)
+        got = out[b, h, torch.tensor(pick, device="cuda")]
+        assert_close(got, ref, torch.bfloat16, f"S={S} causal={causal} (b, h)=({b}, {h})")
+    assert torch.isfinite(out[:, :, ::max(1, S // 1024)].float()).all()

@@ -66,6 +66,12 @@ DECODE = DecodeWorkload("KV-cache decode B64 H32 D128 Skv<=8192 bf16", 64, 32, 8
 
 PREFILL_WORKLOADS = {"tiny_f32": TINY_F32, "prefill": PREFILL, "padded": PADDED, "long": LONG}
 
+# Sequence-length sweep at fixed batch ('Attention from First Principles',
+# Exercises, D: S from 128 to 4096), extended to 65536, where a materialised
+# (B, H, S, S) bf16 score tensor of this batch (2.2 TB) no longer fits in HBM.
+S_SWEEP_SHAPE = dict(B=4, H=32, D=128, seed=5)
+S_SWEEP = (128, 256, 512, 1024, 2048, 4096, 8192, 16384, 32768, 65536)
+
 
 def _normal(shape, gen, device, dtype):
     x = torch.randn(*shape, generator=gen, device=device, dtype=torch.float32)
@@ -118,3 +124,10 @@ def random_tensors(shape, seed, device="cuda", dtype=torch.bfloat16, count=3):
     """``count`` i.i.d. N(0, 1) tensors of one shape from one seed (test helper)."""
     g = _generator(seed, device if str(device).startswith("cuda") else "cpu")
     return [_normal(shape, g, device, dtype) for _ in range(count)]
+
+
+def s_sweep_inputs(S: int, device="cuda", rank: int = 0):
+    """Q, K, V (B, H, S, D) bf16 of the sequence-length sweep at length S."""
+    sh = S_SWEEP_SHAPE
+    g = _generator(sh["seed"] + S + 1000 * rank, device)
+    return [_normal((sh["B"], sh["H"], S, sh["D"]), g, device, torch.bfloat16) for _ in range(3)]
