@@ -10,8 +10,9 @@
 // Persistent kernel, one CTA per SM.  A work item is two 128-row query tiles
 // (Q0, Q1) that read the same key/value head: two consecutive query tiles of
 // one head, or -- grouped-query attention with an even group size -- the same
-// query tile of two heads of one group.  Items are numbered longest-first
-// (causal cost grows with the row) and handed out by an atomic counter, so
+// query tile of two heads of one group.  Items are numbered in blocks of
+// heads whose keys and values fit in part of L2, longest-first inside a block
+// (causal cost grows with the row), and handed out by an atomic counter, so
 // each SM takes the next item when it is ready for it.  Roles (12 warps; the
 // first warpgroup gives registers to the two softmax warpgroups):
 //   warp 0      TMA producer: fetches and decodes the next item, publishes the
@@ -63,6 +64,17 @@ constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr int kItemRing = 4;          // work items in flight between the roles
 constexpr int kItemReaders = 32 + 256;  // MMA warp + both softmax warpgroups
 constexpr int kSchedSlots = 64;       // launches that may run at once with their own counter
+// Bytes of keys and values per block of heads in the item order (see
+// decode_item); 0 puts all heads in one block.
+#ifndef ATTN_L2_GROUP_MB
+#define ATTN_L2_GROUP_MB 16
+#endif
+constexpr long long kL2GroupBytes = static_cast<long long>(ATTN_L2_GROUP_MB) << 20;
+// Work per SM of the last block, in units of the longest item, times 10.
+#ifndef ATTN_TAIL_X10
+#define ATTN_TAIL_X10 20
+#endif
+constexpr long long kTailFactorX10 = ATTN_TAIL_X10;
 
 template <int D>
 struct Layout {
@@ -169,30 +181,47 @@ __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
 __device__ __forceinline__ bool pairs_heads(const FwdArgs &a) { return ((a.H / a.H_kv) & 1) == 0; }
 
-// n_major: query-tile pairs per head (tile pairing) or query tiles (head pairing).
-__device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_major) {
+// Work item t -> (query rows, heads).  The minor index u runs over the M
+// head units (heads, or head pairs of one group), the major index over the
+// n_major query-tile units (query-tile pairs per head with tile pairing, or
+// query tiles with head pairing).  Head units are taken in blocks: the first
+// `front` units in blocks of `group`, the rest as one last block; inside a
+// block the longest rows come first.  A front block's keys and values are
+// sized to stay in L2 while its items run, so the items of one head that run
+// side by side share each K/V tile from L2; the last block is large enough
+// that its longest items still start early (longest-processing-time order
+// at the end of the launch).
+__device__ __forceinline__ Item decode_item(int t, const FwdArgs &a, int n_major, int group, int front) {
     Item it;
     const int G = a.H / a.H_kv;
+    const bool hp = pairs_heads(a);
+    const int M = hp ? a.B * (a.H / 2) : a.B * a.H;
+    int base, cg;
+    if (t < front * n_major) {
+        base = (t / (group * n_major)) * group;
+        cg = group;
+    } else {
+        base = front;
+        cg = M - front;
+    }
+    const int tt = t - base * n_major;
+    const int major = n_major - 1 - tt / cg;  // longest rows first
+    const int u = base + tt % cg;
     int b, h0;
-    if (pairs_heads(a)) {
-        const int HP = a.H / 2, BHP = a.B * HP;
-        const int qt = n_major - 1 - t / BHP;  // longest rows first
-        const int r = t % BHP;
-        b = r / HP;
-        h0 = 2 * (r % HP);
-        it.row_base = qt * kBM;
+    if (hp) {
+        const int HP = a.H / 2;
+        b = u / HP;
+        h0 = 2 * (u % HP);
+        it.row_base = major * kBM;
         it.row_step = 0;
         it.bh_base = b * a.H + h0;
         it.bh_step = 1;
     } else {
-        const int BH = a.B * a.H;
-        const int pair = n_major - 1 - t / BH;  // longest rows first
-        const int bh = t % BH;
-        b = bh / a.H;
-        h0 = bh % a.H;
-        it.row_base = pair * kQTiles * kBM;
+        b = u / a.H;
+        h0 = u % a.H;
+        it.row_base = major * kQTiles * kBM;
         it.row_step = kBM;
-        it.bh_base = bh;
+        it.bh_base = u;
         it.bh_step = 0;
     }
     it.bh_kv = b * a.H_kv + h0 / G;
@@ -268,7 +297,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                      const int n_major, const int n_items, unsigned int *sched) {
+                      const int n_major, const int group, const int front, const int n_items,
+                      unsigned int *sched) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -327,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int t = static_cast<int>(atomicAdd(sched, 1u));
                 Item it;
                 if (t < n_items) {
-                    it = decode_item(t, a, n_major);
+                    it = decode_item(t, a, n_major, group, front);
                 } else {
                     it = Item{0, 0, 0, 0, 0, 0, 0, {0, 0}, -1};
                 }
@@ -791,10 +821,50 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
     if (e != cudaSuccess) return e;
     const long long sms = a.n_sm > 0 ? a.n_sm : 1;
     const unsigned grid = static_cast<unsigned>(n_items < sms ? n_items : sms);
+    // Blocks of the item order (decode_item).  Front blocks hold as many head
+    // units as keep their K and V (a key/value head serves G heads, or G/2
+    // head pairs) within kL2GroupBytes.  The last block holds at least
+    // enough units that its work per SM is kTailFactor times the longest
+    // item; with fewer units than that, one block holds them all.
+    const long long M = head_pairs ? static_cast<long long>(a.B) * (a.H / 2) : static_cast<long long>(a.B) * a.H;
+    long long group = M, front = 0;
+    if (kL2GroupBytes > 0) {
+        const long long units_per_kv = head_pairs ? (a.H / a.H_kv) / 2 : (a.H / a.H_kv);
+        const long long kv_head_bytes = 2LL * a.Skv * D * 2;
+        long long c_l2 = kL2GroupBytes * units_per_kv / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+        c_l2 = c_l2 > 1 ? c_l2 : 1;
+        // K/V steps per head unit and of the longest item, all sequences at full length
+        const int off = a.Skv - a.Sq;
+        long long unit_steps = 0, max_steps = 0;
+        for (int m = 0; m < n_major; ++m) {
+            long long n = 0;
+            for (int x = 0; x < (head_pairs ? 1 : kQTiles); ++x) {
+                const int row0 = head_pairs ? m * kBM : (m * kQTiles + x) * kBM;
+                if (row0 >= a.Sq) continue;
+                const int last = row0 + kBM - 1 < a.Sq - 1 ? row0 + kBM - 1 : a.Sq - 1;
+                int hi = a.causal ? (last + off + 1 < a.Skv ? last + off + 1 : a.Skv) : a.Skv;
+                hi = hi > 0 ? hi : 0;
+                const long long nx = (hi + kBN - 1) / kBN;
+                n = nx > n ? nx : n;
+            }
+            unit_steps += n;
+            max_steps = n > max_steps ? n : max_steps;
+        }
+        const long long c_tail = unit_steps > 0
+            ? (kTailFactorX10 * max_steps * static_cast<long long>(grid) + 10 * unit_steps - 1) / (10 * unit_steps)
+            : M;
+        if (c_l2 < M && c_tail < M) {
+            const long long n_front = (M - c_tail) / c_l2;
+            if (n_front > 0) {
+                group = c_l2;
+                front = n_front * c_l2;
+            }
+        }
+    }
     e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<D><<<grid, kThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv, n_major,
-                                                                      static_cast<int>(n_items), sched);
+    prefill_tc_kernel<D><<<grid, kThreads, L::kSmemBytes, a.stream>>>(
+        a, tq, tk, tv, n_major, static_cast<int>(group), static_cast<int>(front), static_cast<int>(n_items), sched);
     return cudaGetLastError();
 }
 
