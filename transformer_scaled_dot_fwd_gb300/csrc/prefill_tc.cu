@@ -365,34 +365,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars.item_full[slot]);
                 if (it.N < 0) break;
                 TRACE(0, 400 + (k % 100) * 100000, bars.t0);
-                // ---- Q_x, once the previous item's last S MMA on the buffer has completed
-#pragma unroll
-                for (int x = 0; x < kQTiles; ++x) {
-                    if (it.n_kv[x] == 0) continue;
+                // ---- loads in the order the MMA warp consumes them: Q_0, K_0,
+                // Q_1, V_0, K_1, V_1, ...  (Q_1 waits for the previous item's
+                // last S1 to free its buffer; K_0 need not wait for that).
+                // Q_x once the previous item's last S MMA on the buffer has completed:
+                auto load_q = [&](int x) {
+                    if (it.n_kv[x] == 0 || !ok) return;
                     if (q_uses[x] > 0 && !(ok = mbar_wait(&bars.q_empty[x], (q_uses[x] - 1) & 1, &bars.abort)))
-                        break;
+                        return;
                     mbar_arrive_expect_tx(&bars.q_full[x], L::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < L::kSub; ++c)
                         tma_load_3d(smem + x * L::kTileBytes + c * L::kBlockBytes, &tq, &bars.q_full[x], c * 64,
                                     it.row_base + x * it.row_step, it.bh_base + x * it.bh_step);
                     ++q_uses[x];
-                }
-                // ---- K_j, then V_j, through the ring
-                for (int j = 0; j < it.N && ok; ++j) {
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const int s = issued % L::kStages;
-                        if (issued >= L::kStages &&
-                            !(ok = mbar_wait(&bars.kv_empty[s], ((issued / L::kStages) - 1) & 1, &bars.abort)))
-                            break;
-                        TRACE(0, 300 + kv + j * 1000 + (k % 100) * 100000, bars.t0);
-                        mbar_arrive_expect_tx(&bars.kv_full[s], L::kTileBytes);
+                };
+                // K_j (kv = 0) or V_j (kv = 1) into the next ring stage
+                auto load_kv = [&](int j, int kv) {
+                    if (!ok) return;
+                    const int s = issued % L::kStages;
+                    if (issued >= L::kStages &&
+                        !(ok = mbar_wait(&bars.kv_empty[s], ((issued / L::kStages) - 1) & 1, &bars.abort)))
+                        return;
+                    TRACE(0, 300 + kv + j * 1000 + (k % 100) * 100000, bars.t0);
+                    mbar_arrive_expect_tx(&bars.kv_full[s], L::kTileBytes);
 #pragma unroll
-                        for (int c = 0; c < L::kSub; ++c)
-                            tma_load_3d(ring + s * L::kTileBytes + c * L::kBlockBytes, kv ? &tv : &tk,
-                                        &bars.kv_full[s], c * 64, j * kBN, it.bh_kv);
-                        ++issued;
-                    }
+                    for (int c = 0; c < L::kSub; ++c)
+                        tma_load_3d(ring + s * L::kTileBytes + c * L::kBlockBytes, kv ? &tv : &tk, &bars.kv_full[s],
+                                    c * 64, j * kBN, it.bh_kv);
+                    ++issued;
+                };
+                load_q(0);
+                for (int j = 0; j < it.N && ok; ++j) {
+                    load_kv(j, 0);
+                    if (j == 0) load_q(1);
+                    load_kv(j, 1);
                 }
             }
             // never leave with copies still landing in shared memory
@@ -433,6 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t q_uses[kQTiles] = {0, 0}, pr[kQTiles] = {0, 0};
         bool ok = true;
         for (int k = 0; ok; ++k) {
+            TRACE(1, 109 + (k % 100) * 100000, bars.t0);
             Item it;
             if (!(ok = take_item(bars, k, &it))) break;
             release_item(bars, k);
@@ -445,25 +453,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int N = it.N;
             if (N < 0) break;
             if (N == 0) continue;
-#pragma unroll
-            for (int x = 0; x < kQTiles; ++x) {
-                if (it.n_kv[x] == 0) continue;
-                if (!(ok = mbar_wait_warp(&bars.q_full[x], q_uses[x] & 1, &bars.abort))) break;
-                ++q_uses[x];
-            }
-            if (!ok) break;
+            TRACE(1, 110 + (k % 100) * 100000, bars.t0);
+            // S_x_0 per query tile as soon as Q_x and K_0 are in (Q_1 may land
+            // after Q_0: the previous item's last S1 freed its buffer late)
             {
-                const int kslot = consumed % L::kStages;
-                if (!(ok = mbar_wait_warp(&bars.kv_full[kslot], (consumed / L::kStages) & 1, &bars.abort))) break;
-                ++consumed;
-                tc_fence_after();
+                int kslot = 0;
+                bool have_k = false;
 #pragma unroll
-                for (int x = 0; x < kQTiles; ++x)
-                    if (it.n_kv[x] > 0) {
-                        issue_s(x, kslot);
-                        tc_commit_warp(&bars.s_full[x]);
-                        if (it.n_kv[x] == 1) tc_commit_warp(&bars.q_empty[x]);  // last read of Q_x
+                for (int x = 0; x < kQTiles; ++x) {
+                    if (it.n_kv[x] == 0) continue;
+                    if (!(ok = mbar_wait_warp(&bars.q_full[x], q_uses[x] & 1, &bars.abort))) break;
+                    TRACE(1, 111 + 2 * x + (k % 100) * 100000, bars.t0);
+                    ++q_uses[x];
+                    if (!have_k) {
+                        kslot = consumed % L::kStages;
+                        if (!(ok = mbar_wait_warp(&bars.kv_full[kslot], (consumed / L::kStages) & 1, &bars.abort)))
+                            break;
+                        ++consumed;
+                        have_k = true;
                     }
+                    tc_fence_after();
+                    issue_s(x, kslot);
+                    TRACE(1, 112 + 2 * x + (k % 100) * 100000, bars.t0);
+                    tc_commit_warp(&bars.s_full[x]);
+                    if (it.n_kv[x] == 1) tc_commit_warp(&bars.q_empty[x]);  // last read of Q_x
+                }
+                if (!ok) break;
                 tc_commit_warp(&bars.kv_empty[kslot]);
             }
             for (int j = 0; j < N && ok; ++j) {
