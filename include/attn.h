@@ -126,6 +126,37 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
                           const int32_t *kv_len, int dtype, void *stream);
 
 /*
+ * attn_fwd_host -- attn_fwd_gqa with q, k, v, out and kv_len in HOST memory:
+ * the same attention ("Attention from First Principles", section 5 "The full
+ * multi-head computation"), with the copies to and from the GPU done by the
+ * library and overlapped with the computation.
+ *
+ * The batch is cut into chunks of whole key/value-head groups (whole
+ * sequences, or runs of key/value heads of one sequence), each a contiguous
+ * run of (b, h) slices; chunk c is copied in while chunk c - 1 is computed
+ * and chunk c - 2 is copied out, on the library's own copy streams.  Each
+ * chunk is computed exactly as attn_fwd_gqa computes those slices, so the
+ * result equals attn_fwd_gqa's bit for bit.
+ *
+ *   q, k, v, out  host pointers, layouts and sizes as in attn_fwd_gqa.  Page-
+ *                 locked (pinned) memory lets the copies run asynchronously at
+ *                 full speed; pageable memory works but is staged.  out must
+ *                 not overlap the inputs.
+ *   kv_len        NULL or HOST int32[B], meaning as in attn_fwd_gqa.
+ *   stream        the work starts after work already queued on `stream`, which
+ *                 resumes after the last copy out.
+ *
+ * Synchronous: returns when out holds the result (or on error).  D must be 64
+ * or 128 (ATTN_EUNSUPPORTED otherwise).  The library keeps device copies of
+ * q, k, v, out (grown on demand, freed by attn_release), so concurrent calls
+ * on one device run one after the other.  Other errors as in attn_fwd_gqa;
+ * ATTN_ENOMEM if the device copies cannot be allocated.
+ */
+ATTN_API int attn_fwd_host(const void *q, const void *k, const void *v, void *out, int B, int H,
+                           int H_kv, int Sq, int Skv, int D, float scale, int causal,
+                           const int32_t *kv_len, int dtype, void *stream);
+
+/*
  * attn_fwd_chunked -- prefill of a chunk of new queries against a KV cache,
  * with the log-sum-exp of every row.
  *
@@ -289,7 +320,9 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_cycles, void *stream);
 /* Description of the last error on the calling thread ("" if none). */
 ATTN_API const char *attn_last_error(void);
 
-/* Free library-owned device memory (decode workspace) on the current device. */
+/* Free library-owned device memory on the current device: the decode
+ * workspace and attn_fwd_host's device copies.  Not while a call that uses
+ * them is running. */
 ATTN_API void attn_release(void);
 
 #ifdef __cplusplus

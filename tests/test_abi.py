@@ -166,3 +166,12 @@ def test_new_entry_points_reject_bad_arguments(attn_lib):
     # attn_decode_gqa: H_kv must divide H
     assert attn_lib.attn_decode_gqa(Q, K, V, O, 2, 8, 3, 64, 128, None, attn.ATTN_BF16, None) == i
     assert attn.attn_last_error() != ""
+    # attn_fwd_host: the same checks, before any device work
+    assert attn_lib.attn_fwd_host(Q, K, V, O, 2, 6, 4, 16, 16, 128, f(0.1), 1, None, attn.ATTN_BF16, None) == i
+    assert attn_lib.attn_fwd_host(None, K, V, O, 2, 4, 4, 16, 16, 128, f(0.1), 1, None, attn.ATTN_BF16, None) == i
+    assert attn_lib.attn_fwd_host(Q, K, V, O, 2, 4, 4, 17, 16, 128, f(0.1), 1, None, attn.ATTN_BF16, None) == i
+    assert attn_lib.attn_fwd_host(Q, K, V, O, 2, 4, 4, 8, 16, 128, f(0.1), 1, Q, attn.ATTN_BF16, None) == i
+    assert attn_lib.attn_fwd_host(Q, K, V, Q, 2, 4, 4, 16, 16, 128, f(0.1), 1, None, attn.ATTN_BF16, None) == i
+    assert attn_lib.attn_fwd_host(Q, K, V, O, 2, 4, 4, 16, 16, 96, f(0.1), 1, None,
+                                  attn.ATTN_BF16, None) == attn.ATTN_EUNSUPPORTED
+    assert attn_lib.attn_fwd_host(Q, K, V, O, 2, 4, 4, 0, 16, 128, f(0.1), 0, None, attn.ATTN_BF16, None) == 0

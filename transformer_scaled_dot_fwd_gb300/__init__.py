@@ -34,6 +34,7 @@ SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_chunked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
+    "attn_fwd_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_fwd_debug": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "attn_decode": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp]),
     "attn_decode_gqa": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
@@ -163,6 +164,42 @@ def attn_fwd(q, k, v, out=None, scale: Optional[float] = None, causal: bool = Fa
         rc = lib().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, H_kv, Sq, Skv, D,
                                 float(scale), int(bool(causal)), _ptr(kl), _dtype_code(q),
                                 _stream_handle(stream))
+    _check(rc)
+    return out
+
+
+def attn_fwd_host(q, k, v, out=None, scale: Optional[float] = None, causal: bool = False,
+                  kv_len=None, stream=None):
+    """attn_fwd with q, k, v, out in host memory (contiguous CPU tensors; pinned
+    ones copy fastest): the library copies each chunk of heads in, computes it
+    and copies it out, overlapping the three.  kv_len is a CPU int32 tensor of
+    shape (B,) or a sequence of B ints.  Returns ``out`` (allocated like q,
+    pinned if q is, when not given) once it holds the result.  See
+    include/attn.h.
+    """
+    torch = _torch()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D CPU tensor")
+    B, H, Sq, D = q.shape
+    H_kv, Skv = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, H_kv, Skv, D) or tuple(v.shape) != (B, H_kv, Skv, D) or H % H_kv:
+        raise ValueError("k and v must be (B, H_kv, Skv, D) matching q, with H_kv dividing H")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    if out.is_cuda or not out.is_contiguous() or tuple(out.shape) != tuple(q.shape) or out.dtype != q.dtype:
+        raise ValueError("out must be a contiguous CPU tensor matching q")
+    kl = None
+    if kv_len is not None:
+        kl = torch.as_tensor(kv_len, dtype=torch.int32).contiguous()
+        if kl.is_cuda or tuple(kl.shape) != (B,):
+            raise ValueError("kv_len must be B ints on the host")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = lib().attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, H_kv, Sq, Skv, D, float(scale),
+                             int(bool(causal)), _ptr(kl), _dtype_code(q), _stream_handle(stream))
     _check(rc)
     return out
 
@@ -303,7 +340,7 @@ def attn_release() -> None:
 
 
 __all__ = [
-    "attn_fwd", "attn_decode", "attn_decode_noalloc", "attn_decode_splits", "attn_device_status", "attn_release",
+    "attn_fwd", "attn_fwd_chunked", "attn_fwd_debug", "attn_fwd_host", "attn_decode", "attn_decode_noalloc", "attn_decode_splits", "attn_device_status", "attn_release",
     "attn_last_error", "attn_selftest_wait_timeout", "lib", "AttnError", "SIGNATURES", "LIB_PATH",
     "ATTN_F32", "ATTN_BF16", "ATTN_OK", "ATTN_EINVAL", "ATTN_EUNSUPPORTED", "ATTN_ECUDA",
     "ATTN_ENOMEM", "ATTN_ETIMEOUT",

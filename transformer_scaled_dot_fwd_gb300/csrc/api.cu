@@ -156,6 +156,60 @@ int workspace(size_t bytes, void **out) {
     return ATTN_OK;
 }
 
+// ------------------------------------------------------------ host-buffer prefill
+
+// Chunks per call (about) and the smallest chunk worth a copy of its own.
+#ifndef ATTN_HOST_CHUNKS
+#define ATTN_HOST_CHUNKS 8
+#endif
+constexpr int kHostChunks = ATTN_HOST_CHUNKS;
+constexpr size_t kHostMinChunkBytes = 8u << 20;
+constexpr int kHostEvents = 16;  // event pairs in flight; older chunks are waited for
+
+// Per device: device copies of Q, K, V, O and kv_len (grown on demand), the
+// two copy streams and the events that order them with the caller's stream.
+struct HostExec {
+    std::mutex mutex;
+    void *buf = nullptr;
+    size_t bytes = 0;
+    bool ready = false;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev[2 * kHostEvents] = {};
+    cudaEvent_t ev_start = nullptr, ev_end = nullptr;
+
+    int ensure(size_t need) {
+        if (!ready) {
+            cudaError_t e = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking);
+            if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking);
+            for (int i = 0; i < 2 * kHostEvents && e == cudaSuccess; ++i)
+                e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev_end, cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_host: streams and events");
+            ready = true;
+        }
+        if (bytes < need) {
+            if (buf) cudaFree(buf);  // synchronises the device: no call still uses it
+            buf = nullptr;
+            bytes = 0;
+            cudaError_t e = cudaMalloc(&buf, need);
+            if (e != cudaSuccess) {
+                buf = nullptr;
+                return fail(ATTN_ENOMEM, "attn_fwd_host: %zu bytes of device buffers: %s", need, cudaGetErrorString(e));
+            }
+            bytes = need;
+        }
+        return ATTN_OK;
+    }
+    void release() {
+        std::lock_guard<std::mutex> lock(mutex);
+        if (buf) cudaFree(buf);
+        buf = nullptr;
+        bytes = 0;
+    }
+};
+HostExec g_host[kMaxDevices];
+
 // Grouped-query decode: CTAs are (b, h_kv, head subgroup, chunk); the chunk
 // is at most kDecodeGqaMaxChunk keys (the kernel's score buffer).
 int decode_chunk_gqa(int B, int H, int H_kv, int Skv) {
@@ -263,6 +317,101 @@ ATTN_API int attn_fwd_gqa(const void *q, const void *k, const void *v, void *out
                           const int32_t *kv_len, int dtype, void *stream) {
     return fwd_impl(q, k, v, out, nullptr, B, H, H_kv, Sq, Skv, D, scale, causal, kv_len, 0, dtype,
                     stream);
+}
+
+// Prefill from host buffers: the batch is cut into chunks of whole
+// key/value-head groups (runs of consecutive (b, h) slices, contiguous in the
+// (B, H, S, D) layout), and chunk c's copy in, chunk c - 1's attention and
+// chunk c - 2's copy out run at the same time on three streams.
+ATTN_API int attn_fwd_host(const void *q, const void *k, const void *v, void *out, int B, int H,
+                           int H_kv, int Sq, int Skv, int D, float scale, int causal,
+                           const int32_t *kv_len, int dtype, void *stream) {
+    g_last_error[0] = '\0';
+    if (B < 1 || H < 1 || Sq < 0 || Skv < 0)
+        return fail(ATTN_EINVAL, "attn_fwd_host: need B >= 1, H >= 1, Sq >= 0, Skv >= 0");
+    if (H_kv < 1 || H % H_kv != 0)
+        return fail(ATTN_EINVAL, "attn_fwd_host: H_kv must divide H (got H = %d, H_kv = %d)", H, H_kv);
+    if (dtype != ATTN_F32 && dtype != ATTN_BF16) return fail(ATTN_EINVAL, "attn_fwd_host: unknown dtype %d", dtype);
+    if (D != 64 && D != 128) return fail(ATTN_EUNSUPPORTED, "attn_fwd_host: D = %d not supported (64 or 128)", D);
+    if ((Sq > 0 && (!q || !out)) || (Skv > 0 && (!k || !v)))
+        return fail(ATTN_EINVAL, "attn_fwd_host: q and out (Sq > 0), k and v (Skv > 0) must not be NULL");
+    if (causal && Sq > Skv) return fail(ATTN_EINVAL, "attn_fwd_host: causal needs Sq <= Skv (got %d > %d)", Sq, Skv);
+    if (kv_len && causal && Sq != Skv) return fail(ATTN_EINVAL, "attn_fwd_host: causal kv_len needs Sq == Skv");
+    if (Sq == 0) return ATTN_OK;
+    const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
+    const int G = H / H_kv;
+    const size_t q_head = static_cast<size_t>(Sq) * D * esz, kv_head = static_cast<size_t>(Skv) * D * esz;
+    const size_t q_bytes = static_cast<size_t>(B) * H * q_head, kv_bytes = static_cast<size_t>(B) * H_kv * kv_head;
+    if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) || overlaps(out, q_bytes, v, kv_bytes))
+        return fail(ATTN_EINVAL, "attn_fwd_host: out overlaps an input");
+    int dev;
+    int rc = current_device(&dev);
+    if (rc) return rc;
+    HostExec &x = g_host[dev];
+    std::lock_guard<std::mutex> lock(x.mutex);  // one call at a time per device: it owns the buffers
+    // device copies: Q | K | V | O | kv_len, each 256-byte aligned
+    auto up = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
+    const size_t off_k = up(q_bytes), off_v = off_k + up(kv_bytes), off_o = off_v + up(kv_bytes);
+    const size_t off_l = off_o + up(q_bytes), total = off_l + up(static_cast<size_t>(B) * sizeof(int32_t));
+    if ((rc = x.ensure(total))) return rc;
+    char *dbuf = static_cast<char *>(x.buf);
+    int32_t *d_len = kv_len ? reinterpret_cast<int32_t *>(dbuf + off_l) : nullptr;
+    // chunks: whole batches when one batch is below the target, else runs of key/value heads of one batch
+    const size_t per_b = static_cast<size_t>(H) * q_head + 2 * static_cast<size_t>(H_kv) * kv_head;
+    size_t target = (static_cast<size_t>(B) * per_b) / kHostChunks;
+    target = target < kHostMinChunkBytes ? kHostMinChunkBytes : target;
+    int nb = 1, kv_per = H_kv;  // batches per chunk, or key/value heads per chunk (nb == 1)
+    if (per_b <= target) {
+        nb = static_cast<int>(target / per_b);
+        nb = nb < 1 ? 1 : (nb > B ? B : nb);
+    } else {
+        const size_t per_kv = static_cast<size_t>(G) * q_head + 2 * kv_head;
+        kv_per = static_cast<int>((target + per_kv - 1) / per_kv);
+        kv_per = kv_per < 1 ? 1 : (kv_per > H_kv ? H_kv : kv_per);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaEventRecord(x.ev_start, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(x.h2d, x.ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(x.d2h, x.ev_start, 0);
+    if (e == cudaSuccess && kv_len)
+        e = cudaMemcpyAsync(d_len, kv_len, static_cast<size_t>(B) * sizeof(int32_t), cudaMemcpyHostToDevice, x.h2d);
+    int n_chunk = 0;
+    for (int b0 = 0; b0 < B && e == cudaSuccess && rc == ATTN_OK; b0 += nb) {
+        const int bn = b0 + nb <= B ? nb : B - b0;
+        for (int g0 = 0; g0 < H_kv && e == cudaSuccess && rc == ATTN_OK; g0 += kv_per) {
+            const int gn = g0 + kv_per <= H_kv ? kv_per : H_kv - g0;
+            // slices: batches [b0, b0 + bn) x kv heads [g0, g0 + gn) (nb == 1 or gn == H_kv)
+            const size_t qo = (static_cast<size_t>(b0) * H + static_cast<size_t>(g0) * G) * q_head;
+            const size_t ko = (static_cast<size_t>(b0) * H_kv + g0) * kv_head;
+            const size_t qn = static_cast<size_t>(bn) * gn * G * q_head, kn = static_cast<size_t>(bn) * gn * kv_head;
+            cudaEvent_t ev_in = x.ev[2 * (n_chunk % kHostEvents)], ev_done = x.ev[2 * (n_chunk % kHostEvents) + 1];
+            if (n_chunk >= kHostEvents) e = cudaEventSynchronize(x.ev[2 * (n_chunk % kHostEvents) + 1]);
+            if (e == cudaSuccess) e = cudaMemcpyAsync(dbuf + qo, static_cast<const char *>(q) + qo, qn, cudaMemcpyHostToDevice, x.h2d);
+            if (e == cudaSuccess && Skv > 0)
+                e = cudaMemcpyAsync(dbuf + off_k + ko, static_cast<const char *>(k) + ko, kn, cudaMemcpyHostToDevice, x.h2d);
+            if (e == cudaSuccess && Skv > 0)
+                e = cudaMemcpyAsync(dbuf + off_v + ko, static_cast<const char *>(v) + ko, kn, cudaMemcpyHostToDevice, x.h2d);
+            if (e == cudaSuccess) e = cudaEventRecord(ev_in, x.h2d);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in, 0);
+            if (e != cudaSuccess) break;
+            rc = fwd_impl(dbuf + qo, dbuf + off_k + ko, dbuf + off_v + ko, dbuf + off_o + qo, nullptr, bn,
+                          gn * G, gn, Sq, Skv, D, scale, causal, d_len ? d_len + b0 : nullptr, 0, dtype, st);
+            if (rc) break;
+            e = cudaEventRecord(ev_done, st);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(x.d2h, ev_done, 0);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(static_cast<char *>(out) + qo, dbuf + off_o + qo, qn, cudaMemcpyDeviceToHost, x.d2h);
+            ++n_chunk;
+        }
+    }
+    // the caller's stream resumes after the last copy out; the call returns when it is done
+    cudaError_t e2 = cudaEventRecord(x.ev_end, x.d2h);
+    if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(st, x.ev_end, 0);
+    if (e2 == cudaSuccess) e2 = cudaEventSynchronize(x.ev_end);
+    if (rc) return rc;
+    if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_host");
+    if (e2 != cudaSuccess) return cuda_fail(e2, "attn_fwd_host (completion)");
+    return ATTN_OK;
 }
 
 ATTN_API int attn_fwd_chunked(const void *q, const void *kcache, const void *vcache, void *out,
@@ -446,10 +595,14 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_cycles, void *stream) {
 ATTN_API void attn_release(void) {
     int dev;
     if (current_device(&dev)) return;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_ws[dev].ptr) cudaFree(g_ws[dev].ptr);
-    g_ws[dev].ptr = nullptr;
-    g_ws[dev].bytes = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (g_ws[dev].ptr) cudaFree(g_ws[dev].ptr);
+        g_ws[dev].ptr = nullptr;
+        g_ws[dev].bytes = 0;
+    }
+    // outside g_mutex: attn_fwd_host takes its own lock first, then g_mutex
+    g_host[dev].release();
 }
 
 }  // extern "C"
