@@ -107,9 +107,9 @@ int get_encode(EncodeTiledFn *fn) {
     return ATTN_OK;
 }
 
-// (D, S, B*H) bf16 view of a (B, H, S, D) tensor; boxes of 64 x 128 x 1 with
-// 128-byte swizzle, out-of-range rows read as zero.
-int make_map(CUtensorMap *map, const void *base, int D, int S, long long BH) {
+// (D, S, B*H) bf16 view of a (B, H, S, D) tensor; boxes of 64 x box_rows x 1
+// with 128-byte swizzle, out-of-range rows read as zero.
+int make_map(CUtensorMap *map, const void *base, int D, int S, long long BH, int box_rows = 128) {
     EncodeTiledFn encode;
     int rc = get_encode(&encode);
     if (rc) return rc;
@@ -117,13 +117,30 @@ int make_map(CUtensorMap *map, const void *base, int D, int S, long long BH) {
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
                                    static_cast<cuuint64_t>(S) * D * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ATTN_ECUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return ATTN_OK;
+}
+
+// (D, rows) bf16 view of a row-major (rows, D) tensor; boxes of 64 x 128 with
+// 128-byte swizzle, rows past the end read as zero.
+int make_map_rows(CUtensorMap *map, const void *base, int D, long long rows) {
+    EncodeTiledFn encode;
+    int rc = get_encode(&encode);
+    if (rc) return rc;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ATTN_ECUDA, "cuTensorMapEncodeTiled (2-D) failed (%d)", static_cast<int>(r));
     return ATTN_OK;
 }
 
@@ -504,7 +521,11 @@ ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcac
         overlaps(out, qo_bytes, vcache, kv_bytes))
         return fail(ATTN_EINVAL, "attn_decode: out overlaps an input");
 
-    const int chunk = H_kv == H ? decode_chunk(B, H, Skv) : decode_chunk_gqa(B, H, H_kv, Skv);
+    // large query groups: the tensor-core kernel (the group's queries are the rows of one tile)
+    const int G = H / H_kv;
+    const bool tc = G >= kDecodeTcMinGroup && G <= 128 && bh_kv <= 65535;
+    const int chunk = tc ? decode_tc_chunk(B, H_kv, Skv, num_sms())
+                         : (H_kv == H ? decode_chunk(B, H, Skv) : decode_chunk_gqa(B, H, H_kv, Skv));
     const int n_split = Skv > 0 ? (Skv + chunk - 1) / chunk : 1;
     const size_t o_bytes = static_cast<size_t>(bh) * n_split * D * sizeof(float);
     const size_t ml_bytes = static_cast<size_t>(bh) * n_split * 2 * sizeof(float);
@@ -517,7 +538,16 @@ ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcac
                  chunk, n_split, static_cast<float *>(ws),
                  reinterpret_cast<float *>(static_cast<char *>(ws) + o_bytes), status,
                  static_cast<cudaStream_t>(stream), H_kv};
-    cudaError_t e = H_kv == H ? launch_decode(a) : launch_decode_gqa(a);
+    cudaError_t e;
+    if (tc) {
+        CUtensorMap tq, tk, tv;
+        if (Skv > 0 && ((rc = make_map_rows(&tq, q, D, bh)) || (rc = make_map(&tk, kcache, D, Skv, bh_kv, 64)) ||
+                        (rc = make_map(&tv, vcache, D, Skv, bh_kv, 64))))
+            return rc;
+        e = launch_decode_tc(a, tq, tk, tv);
+    } else {
+        e = H_kv == H ? launch_decode(a) : launch_decode_gqa(a);
+    }
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode launch");
 }
 

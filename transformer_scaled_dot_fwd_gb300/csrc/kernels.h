@@ -79,6 +79,21 @@ cudaError_t launch_decode_combine(const DecodeArgs &a);
 cudaError_t launch_decode_gqa(const DecodeArgs &a);
 int decode_gqa_heads_per_cta(int G);
 
+// Grouped-query / multi-query decode on the tensor cores (G = H / H_kv query
+// heads per cached head, kDecodeTcMinGroup <= G <= 128; below that the CUDA-core
+// kernels are as fast or faster): the G queries are the
+// rows of one 128-row tile.  tq views q as (D, B*H) with 64 x 128 boxes; tk, tv
+// view the caches as (D, Skv, B*H_kv) with 64 x 64 x 1 boxes (128-byte swizzle).
+// a.chunk (a multiple of 64 keys, from decode_tc_chunk) and a.n_split as for
+// the other decode kernels; the partials are merged by the decode combine.
+#ifndef ATTN_DTC_MIN_GROUP
+#define ATTN_DTC_MIN_GROUP 4
+#endif
+constexpr int kDecodeTcMinGroup = ATTN_DTC_MIN_GROUP;
+int decode_tc_chunk(int B, int H_kv, int Skv, int n_sm);
+cudaError_t launch_decode_tc(const DecodeArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv);
+
 // Size of the library-static decode scratch used by attn_decode_noalloc.
 constexpr size_t kDecodeNoAllocScratchBytes = 32u << 20;
 
