@@ -440,7 +440,7 @@ def run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, ra
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     lens = wl.draw_lengths(B, dwk.kv_len_range, dwk.seed + 1000 * rank).tolist()
     kl = torch.tensor(lens, dtype=torch.int32, device=device)
-    for H_kv in (dwk.H, 8, 1):
+    for H_kv in (args.decode_hkv or (dwk.H, 8, 1)):
         g = torch.Generator(device=device).manual_seed(dwk.seed + H_kv)
         q = torch.randn(B, dwk.H, dwk.D, device=device, generator=g).to(torch.bfloat16)
         kc = torch.randn(B, H_kv, dwk.Skv, dwk.D, device=device, generator=g).to(torch.bfloat16)
@@ -600,6 +600,8 @@ def main():
                     "prefill against sequence length")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="profiling runs: smaller decode batch than the workload's 64")
+    ap.add_argument("--decode-hkv", type=lambda x: [int(v) for v in x.split(",")], default=None,
+                    help="decode-gqa runs: comma-separated key/value head counts (default 32,8,1)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
