@@ -7,10 +7,17 @@ One step is one attn_fwd call on the prefill workload (the headline `value`),
 timed with CUDA events on the launching stream, L2 flushed between steps
 outside the events.  The decode workload (B64 H32 D128, cache padded to 8192,
 lengths uniform on [4096, 8192]) is timed the same way and reported under
-"decode".  Rank 0 prints one JSON line.
+"decode".  "e2e" is the same prefill through attn_fwd_host from pinned host
+buffers, copies inside the timed call.  Rank 0 prints one JSON line.
 
 --impl reference times the fp64 CPU checker (the only reference this method
 has) on a bounded sample of the same workload, on the host cores.
+
+Profiling and extra runs (not part of the default line):
+    --only prefill | decode        one kernel family
+    --only decode-gqa [--decode-hkv 32,8,1]
+                                   grouped-query decode on the decode workload's shape
+    --only s-sweep                 prefill time against sequence length (S = 128 .. 65536)
 
 Under torchrun (N > 1) each rank runs its own shard of the global batch
 (sequences are independent problems: no data-path collective); the process
