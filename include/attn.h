@@ -226,7 +226,8 @@ ATTN_API int attn_fwd_debug(const void *q, const void *k, const void *v, void *o
  *   out     (B, H, D)        written
  *   kv_len  NULL (every sequence uses all Skv positions) or device int32[B];
  *           keys j >= kv_len[b] are ignored, kv_len[b] == 0 gives zeros.
- *   dtype   ATTN_BF16 only; D must be 64 or 128.
+ *   dtype   ATTN_BF16 or ATTN_F32 (fp32 everywhere, on the CUDA cores); D
+ *           must be 64 or 128.  All pointers 16-byte aligned.
  *
  * The kernel splits each sequence's keys into chunks processed in parallel
  * and merges the partial softmax results; the partials live in a workspace
@@ -254,7 +255,9 @@ ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, 
  *
  * Every other argument, rule, error and the workspace behaviour are as in
  * attn_decode; H_kv < 1 or H not a multiple of H_kv returns ATTN_EINVAL.
- * H_kv == H runs attn_decode's kernels.
+ * H_kv == H runs attn_decode's kernels.  In bf16, groups of G = H / H_kv >= 4
+ * heads (up to 128) run on the tensor cores, the group's queries forming the
+ * rows of one tile; smaller groups and fp32 run on the CUDA cores.
  */
 ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcache, void *out, int B,
                              int H, int H_kv, int Skv, int D, const int32_t *kv_len, int dtype,

@@ -93,7 +93,7 @@ def dec(lib, q=Q, k=K, v=V, o=O, B=2, H=2, Skv=64, D=128, kl=None, dtype=attn.AT
     (dict(Skv=-1), attn.ATTN_EINVAL),
     (dict(D=-4), attn.ATTN_EINVAL),
     (dict(D=80), attn.ATTN_EUNSUPPORTED),
-    (dict(dtype=attn.ATTN_F32), attn.ATTN_EUNSUPPORTED),
+    (dict(dtype=attn.ATTN_F32, D=80), attn.ATTN_EUNSUPPORTED),
     (dict(dtype=3), attn.ATTN_EINVAL),
     (dict(v=ctypes.c_void_p(0x30000004)), attn.ATTN_EINVAL),
     (dict(o=ctypes.c_void_p(0x10000000 + 256)), attn.ATTN_EINVAL),

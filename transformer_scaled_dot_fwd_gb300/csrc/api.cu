@@ -505,7 +505,6 @@ ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcac
         return fail(ATTN_EINVAL, "attn_decode: q, out and (for Skv > 0) kcache, vcache must not be NULL");
     if (dtype != ATTN_F32 && dtype != ATTN_BF16) return fail(ATTN_EINVAL, "attn_decode: unknown dtype %d", dtype);
     if (D <= 0) return fail(ATTN_EINVAL, "attn_decode: D must be positive (got %d)", D);
-    if (dtype != ATTN_BF16) return fail(ATTN_EUNSUPPORTED, "attn_decode: only bf16 is implemented");
     if (D != 64 && D != 128) return fail(ATTN_EUNSUPPORTED, "attn_decode: D = %d not supported (64 or 128)", D);
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
         return fail(ATTN_EINVAL, "attn_decode: q, kcache, vcache and out must be 16-byte aligned");
@@ -515,17 +514,20 @@ ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcac
     const long long bh_kv = static_cast<long long>(B) * H_kv;
     if (bh * (Skv > 1 ? Skv : 1) >= (1LL << 31) || bh >= (1LL << 31) / 64)
         return fail(ATTN_EINVAL, "attn_decode: B*H*Skv is too large");
-    const size_t qo_bytes = static_cast<size_t>(bh) * D * 2;
-    const size_t kv_bytes = static_cast<size_t>(bh_kv) * Skv * D * 2;
+    const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
+    const size_t qo_bytes = static_cast<size_t>(bh) * D * esz;
+    const size_t kv_bytes = static_cast<size_t>(bh_kv) * Skv * D * esz;
     if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, kcache, kv_bytes) ||
         overlaps(out, qo_bytes, vcache, kv_bytes))
         return fail(ATTN_EINVAL, "attn_decode: out overlaps an input");
 
-    // large query groups: the tensor-core kernel (the group's queries are the rows of one tile)
+    // bf16 with large query groups: the tensor-core kernel (the group's queries
+    // are the rows of one tile); fp32: its own CUDA-core kernel
+    const bool f32 = dtype == ATTN_F32;
     const int G = H / H_kv;
-    const bool tc = G >= kDecodeTcMinGroup && G <= 128 && bh_kv <= 65535;
+    const bool tc = !f32 && G >= kDecodeTcMinGroup && G <= 128 && bh_kv <= 65535;
     const int chunk = tc ? decode_tc_chunk(B, H_kv, Skv, num_sms())
-                         : (H_kv == H ? decode_chunk(B, H, Skv) : decode_chunk_gqa(B, H, H_kv, Skv));
+                         : ((H_kv == H || f32) ? decode_chunk(B, H, Skv) : decode_chunk_gqa(B, H, H_kv, Skv));
     const int n_split = Skv > 0 ? (Skv + chunk - 1) / chunk : 1;
     const size_t o_bytes = static_cast<size_t>(bh) * n_split * D * sizeof(float);
     const size_t ml_bytes = static_cast<size_t>(bh) * n_split * 2 * sizeof(float);
@@ -545,6 +547,8 @@ ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcac
                         (rc = make_map(&tv, vcache, D, Skv, bh_kv, 64))))
             return rc;
         e = launch_decode_tc(a, tq, tk, tv);
+    } else if (f32) {
+        e = launch_decode_f32(a);
     } else {
         e = H_kv == H ? launch_decode(a) : launch_decode_gqa(a);
     }
@@ -561,7 +565,6 @@ ATTN_API int attn_decode_noalloc(const void *q, const void *kcache, const void *
     if (dtype != ATTN_F32 && dtype != ATTN_BF16)
         return fail(ATTN_EINVAL, "attn_decode_noalloc: unknown dtype %d", dtype);
     if (D <= 0) return fail(ATTN_EINVAL, "attn_decode_noalloc: D must be positive (got %d)", D);
-    if (dtype != ATTN_BF16) return fail(ATTN_EUNSUPPORTED, "attn_decode_noalloc: only bf16 is implemented");
     if (D != 64 && D != 128)
         return fail(ATTN_EUNSUPPORTED, "attn_decode_noalloc: D = %d not supported (64 or 128)", D);
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(out))
@@ -571,8 +574,9 @@ ATTN_API int attn_decode_noalloc(const void *q, const void *kcache, const void *
     const long long bh = static_cast<long long>(B) * H;
     if (bh * (Skv > 1 ? Skv : 1) >= (1LL << 31) || bh >= (1LL << 31) / 64)
         return fail(ATTN_EINVAL, "attn_decode_noalloc: B*H*Skv is too large");
-    const size_t qo_bytes = static_cast<size_t>(bh) * D * 2;
-    const size_t kv_bytes = static_cast<size_t>(bh) * Skv * D * 2;
+    const size_t esz = dtype == ATTN_BF16 ? 2 : 4;
+    const size_t qo_bytes = static_cast<size_t>(bh) * D * esz;
+    const size_t kv_bytes = static_cast<size_t>(bh) * Skv * D * esz;
     if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, kcache, kv_bytes) ||
         overlaps(out, qo_bytes, vcache, kv_bytes))
         return fail(ATTN_EINVAL, "attn_decode_noalloc: out overlaps an input");
@@ -589,7 +593,7 @@ ATTN_API int attn_decode_noalloc(const void *q, const void *kcache, const void *
     if (rc) return rc;
     DecodeArgs a{q, kcache, vcache, out, kv_len, B, H, Skv, D, 1.0f / sqrtf(static_cast<float>(D)),
                  chunk, n_split, nullptr, nullptr, status, static_cast<cudaStream_t>(stream), H};
-    cudaError_t e = launch_decode_noalloc(a);
+    cudaError_t e = launch_decode_noalloc(a, dtype == ATTN_F32);
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_decode_noalloc launch");
 }
 

@@ -44,17 +44,17 @@ cudaError_t decode_noalloc_scratch(void **out) {
     return cudaSuccess;
 }
 
-// The regular decode kernels, with their partials in the static scratch.  The
-// partials need no clearing: every chunk the combine step reads is written by
-// the same call first.
-cudaError_t launch_decode_noalloc(DecodeArgs a) {
+// The regular decode kernels (bf16, or fp32 when f32), with their partials in
+// the static scratch.  The partials need no clearing: every chunk the combine
+// step reads is written by the same call first.
+cudaError_t launch_decode_noalloc(DecodeArgs a, bool f32) {
     void *scratch = nullptr;
     cudaError_t e = decode_noalloc_scratch(&scratch);
     if (e != cudaSuccess) return e;
     const size_t o_bytes = static_cast<size_t>(a.B) * a.H * a.n_split * a.D * sizeof(float);
     a.part_o = static_cast<float *>(scratch);
     a.part_ml = reinterpret_cast<float *>(static_cast<unsigned char *>(scratch) + o_bytes);
-    return launch_decode(a);
+    return f32 ? launch_decode_f32(a) : launch_decode(a);
 }
 
 }  // namespace attn

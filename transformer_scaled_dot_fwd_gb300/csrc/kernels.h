@@ -27,9 +27,9 @@ struct FwdArgs {
 };
 
 struct DecodeArgs {
-    const void *q;          // (B, H, D) bf16
-    const void *k, *v;      // (B, H, Skv, D) bf16
-    void *out;              // (B, H, D) bf16
+    const void *q;          // (B, H, D) bf16 (fp32 for launch_decode_f32)
+    const void *k, *v;      // (B, H_kv, Skv, D), same dtype
+    void *out;              // (B, H, D), same dtype
     const int32_t *kv_len;  // device int32[B] or nullptr
     int B, H, Skv, D;
     float scale;
@@ -79,6 +79,11 @@ cudaError_t launch_decode_combine(const DecodeArgs &a);
 cudaError_t launch_decode_gqa(const DecodeArgs &a);
 int decode_gqa_heads_per_cta(int G);
 
+// fp32 decode (any grouping H_kv | H): q, caches and out are fp32; partial
+// kernel per (b, h, chunk <= kDecodeMaxChunk keys) on the CUDA cores, then an
+// fp32-output combine.
+cudaError_t launch_decode_f32(const DecodeArgs &a);
+
 // Grouped-query / multi-query decode on the tensor cores (G = H / H_kv query
 // heads per cached head, kDecodeTcMinGroup <= G <= 128; below that the CUDA-core
 // kernels are as fast or faster): the G queries are the
@@ -99,7 +104,7 @@ constexpr size_t kDecodeNoAllocScratchBytes = 32u << 20;
 
 // Decode with its partials in the library-static scratch (no allocation).
 // The caller has checked that the partials fit in kDecodeNoAllocScratchBytes.
-cudaError_t launch_decode_noalloc(DecodeArgs a);
+cudaError_t launch_decode_noalloc(DecodeArgs a, bool f32);
 
 // One-warp kernel whose only wait can never complete: exercises the bounded
 // wait and the status word (attn_selftest_wait_timeout).
