@@ -298,6 +298,20 @@ def run_reference(args):
     return 0
 
 
+def run_env(device, seeds):
+    """Versions and seeds behind a measurement."""
+    driver = None
+    try:
+        r = subprocess.run(["nvidia-smi", "-i", str(device.index or 0), "--query-gpu=driver_version",
+                            "--format=csv,noheader"], capture_output=True, text=True, timeout=10)
+        driver = r.stdout.strip() or None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"torch": torch.__version__, "cuda_runtime": torch.version.cuda, "driver": driver,
+            "device": torch.cuda.get_device_name(device), "sms": torch.cuda.get_device_properties(device).multi_processor_count,
+            "seeds": seeds}
+
+
 def config_dict(w, world):
     return {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "causal": w.causal,
             "global_batch": w.B * world, "seq_len": w.S,
@@ -389,6 +403,7 @@ def run_ours(args):
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
         "clocks": clocks, "gpu_launches": args.steps,
         "wall_s_timed_region": wall, "kernel_source_digest": kernel_source_digest(),
+        "env": run_env(device, {"prefill": w.seed, "decode": wl.DECODE.seed, "rank_offset": 1000}),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
