@@ -44,6 +44,7 @@ struct __align__(128) DecodeSmem {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_partial_kernel(DecodeArgs a) {
+    griddep_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem<D> &sm = *reinterpret_cast<DecodeSmem<D> *>(smem_raw);
 
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(DecodeArgs a) 
 
 template <int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
+    griddep_wait();  // the partial kernel's results (launched early: see launch_decode_combine)
     const int bh = blockIdx.x;
     const int d = threadIdx.x;
     const int b = bh / a.H;
@@ -268,12 +270,25 @@ cudaError_t launch_decode_t(const DecodeArgs &a) {
 
 }  // namespace
 
+// The combine is launched with programmatic stream serialization: once every
+// CTA of the partial kernel has started (each signals at its start), the
+// combine's blocks may be placed and wait in griddep_wait for the partial
+// kernel to finish, which hides the launch gap between the two kernels.
 cudaError_t launch_decode_combine(const DecodeArgs &a) {
-    if (a.D == 64)
-        decode_combine_kernel<64><<<a.B * a.H, 64, 0, a.stream>>>(a);
-    else
-        decode_combine_kernel<128><<<a.B * a.H, 128, 0, a.stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.H));
+    cfg.blockDim = dim3(static_cast<unsigned>(a.D));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+#ifndef ATTN_NO_PDL
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#endif
+    return a.D == 64 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<64>, a)
+                     : cudaLaunchKernelEx(&cfg, decode_combine_kernel<128>, a);
 }
 
 cudaError_t launch_decode(const DecodeArgs &a) {

@@ -48,6 +48,7 @@ struct __align__(128) GqaSmem {
 
 template <int D, int GT>
 __global__ void __launch_bounds__(kThreads) decode_gqa_partial_kernel(DecodeArgs a, int n_sub) {
+    griddep_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem_raw[];
     GqaSmem<D, GT> &sm = *reinterpret_cast<GqaSmem<D, GT> *>(smem_raw);
 

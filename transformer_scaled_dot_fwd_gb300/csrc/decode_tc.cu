@@ -80,6 +80,7 @@ template <int D>
 __global__ void __launch_bounds__(kTcThreads, kTcMinBlocks)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tq,
                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
+    griddep_launch_dependents();  // the combine may be placed once every CTA has started
     using L = TcLayout<D>;
     const int c = blockIdx.x;   // chunk of keys
     const int bk = blockIdx.y;  // b * H_kv + h_kv

@@ -103,6 +103,16 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization waits here until the previous kernel in the stream has
+// finished and its writes are visible (a no-op when launched without it).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be launched once every CTA of this grid
+// has signalled (or exited); its CTAs then wait in griddep_wait.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over a subset of the CTA's warps.
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
