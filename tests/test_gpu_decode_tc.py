@@ -47,6 +47,24 @@ def test_large_group_decode_lengths(gpu, H, H_kv):
     assert torch.count_nonzero(out[1]) == 0  # a sequence with no keys gives zeros
 
 
+@pytest.mark.parametrize("B,H,H_kv,Skv,kind", [
+    (1, 32, 1, 20000, "full"),          # one long sequence: many chunks of one cached head
+    (300, 8, 2, 200, "random"),         # many short sequences of random length
+    (5, 16, 4, 700, "empty"),           # no keys at all: every output is zero
+    (70, 32, 8, 129, "mostly_empty"),   # few keys in the whole batch
+    (3, 64, 16, 4096, "ragged"),        # sequences of very different lengths
+])
+def test_batch_shapes(gpu, B, H, H_kv, Skv, kind):
+    rng = np.random.default_rng(B + Skv)
+    lens = {"full": [Skv] * B, "random": rng.integers(0, Skv + 1, B).tolist(), "empty": [0] * B,
+            "mostly_empty": [0] * (B - 3) + [1, 64, Skv], "ragged": [Skv, 1, 777]}[kind]
+    out, ref = _case(B, H, H_kv, Skv, 128, lens=lens, seed=B * 7 + H)
+    assert_close(out, ref, torch.bfloat16, f"batch B={B} H={H} H_kv={H_kv} Skv={Skv} {kind}")
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert torch.count_nonzero(out[b]) == 0
+
+
 def test_growing_scores_rescale_mid_stream(gpu):
     """Keys scaled up along the cache: each later tile's scores exceed the
     running max by more than 2^8, so O is rescaled again and again."""
