@@ -227,31 +227,102 @@ __global__ void __launch_bounds__(kThreads) decode_partial_kernel(DecodeArgs a) 
     }
 }
 
+// One warp per (b, h) row, four rows per block: lane t owns output dims
+// [t * D/32, (t + 1) * D/32).  Chunk maxima and sums are spread over the
+// lanes and each chunk's weight is broadcast to the warp; the partial loads
+// of 16 chunks carry no branch, so they are all in flight together.
+constexpr int kCombineRows = 4;
+
 template <int D>
-__global__ void __launch_bounds__(D) decode_combine_kernel(DecodeArgs a) {
-    griddep_wait();  // the partial kernel's results (launched early: see launch_decode_combine)
-    const int bh = blockIdx.x;
-    const int d = threadIdx.x;
-    const int b = bh / a.H;
+__global__ void __launch_bounds__(32 * kCombineRows) decode_combine_kernel(DecodeArgs a) {
+    constexpr int kV = D / 32;  // output dims per lane
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kCombineRows + (threadIdx.x >> 5);  // b * H + h
+    const bool live = row < a.B * a.H;
     int L = a.Skv;
-    if (a.kv_len) L = min(max(a.kv_len[b], 0), a.Skv);
+    if (live && a.kv_len) L = min(max(a.kv_len[row / a.H], 0), a.Skv);  // an input: read before the wait
+    griddep_wait();  // the partial kernel's results (launched early: see launch_decode_combine)
+    if (!live) return;
     const int nv = (L + a.chunk - 1) / a.chunk;  // chunks holding at least one key
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + static_cast<size_t>(bh) * D;
-    if (nv == 0) {
-        out[d] = __float2bfloat16_rn(0.f);
-        return;
+    const float *ml = a.part_ml + static_cast<size_t>(row) * a.n_split * 2;
+    const float *po = a.part_o + static_cast<size_t>(row) * a.n_split * D + lane * kV;
+    float acc[kV], lsum = 0.f;
+#pragma unroll
+    for (int e = 0; e < kV; ++e) acc[e] = 0.f;
+    // The partial outputs of 16 chunks, c0 .. c0 + 15: a load past the last
+    // chunk re-reads that chunk (a valid address) and later gets weight 0, so
+    // the loads carry no branch and are all in flight together.
+    float v[16][kV];
+    auto load16 = [&](int c0) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float *p = po + static_cast<size_t>(min(c0 + i, nv - 1)) * D;
+            if constexpr (kV == 4) {
+                const float4 t = *reinterpret_cast<const float4 *>(p);
+                v[i][0] = t.x;
+                v[i][1] = t.y;
+                v[i][2] = t.z;
+                v[i][3] = t.w;
+            } else {
+                const float2 t = *reinterpret_cast<const float2 *>(p);
+                v[i][0] = t.x;
+                v[i][1] = t.y;
+            }
+        }
+    };
+    // chunk c0 + i carries the weight held by lane i
+    auto mix16 = [&](float w) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float wi = __shfl_sync(0xffffffffu, w, i);
+#pragma unroll
+            for (int e = 0; e < kV; ++e) acc[e] = fmaf(wi, v[i][e], acc[e]);
+        }
+    };
+    if (nv > 0 && nv <= 16) {
+        // one round of loads: the chunk statistics and outputs together
+        float mc = -INFINITY, lc = 0.f;
+        if (lane < nv) {
+            mc = ml[2 * lane];
+            lc = ml[2 * lane + 1];
+        }
+        load16(0);
+        float M = mc;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float w = lane < nv ? ex2_approx(mc - M) : 0.f;
+        lsum = w * lc;
+        mix16(w);
+    } else if (nv > 16) {
+        float M = -INFINITY;
+        for (int c = lane; c < nv; c += 32) M = fmaxf(M, ml[2 * c]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        for (int c0 = 0; c0 < nv; c0 += 16) {
+            const int c = c0 + lane;
+            float w = 0.f;
+            if (lane < 16 && c < nv) {
+                w = ex2_approx(ml[2 * c] - M);
+                lsum = fmaf(w, ml[2 * c + 1], lsum);
+            }
+            load16(c0);
+            mix16(w);
+        }
     }
-    const float *ml = a.part_ml + static_cast<size_t>(bh) * a.n_split * 2;
-    const float *po = a.part_o + static_cast<size_t>(bh) * a.n_split * D;
-    float M = -INFINITY;
-    for (int c = 0; c < nv; ++c) M = fmaxf(M, ml[2 * c]);
-    float acc = 0.f, lsum = 0.f;
-    for (int c = 0; c < nv; ++c) {
-        const float w = ex2_approx(ml[2 * c] - M);
-        acc = fmaf(w, po[static_cast<size_t>(c) * D + d], acc);
-        lsum = fmaf(w, ml[2 * c + 1], lsum);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+    const float inv = nv > 0 ? 1.f / lsum : 0.f;  // no key: exact zeros
+    uint32_t pk[kV / 2];
+#pragma unroll
+    for (int e = 0; e < kV / 2; ++e) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+        pk[e] = *reinterpret_cast<uint32_t *>(&h2);
     }
-    out[d] = __float2bfloat16_rn(acc / lsum);
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + static_cast<size_t>(row) * D + lane * kV;
+    if constexpr (kV == 4)
+        *reinterpret_cast<uint2 *>(out) = make_uint2(pk[0], pk[1]);
+    else
+        *reinterpret_cast<uint32_t *>(out) = pk[0];
 }
 
 template <int D>
@@ -276,8 +347,8 @@ cudaError_t launch_decode_t(const DecodeArgs &a) {
 // kernel to finish, which hides the launch gap between the two kernels.
 cudaError_t launch_decode_combine(const DecodeArgs &a) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.B * a.H));
-    cfg.blockDim = dim3(static_cast<unsigned>(a.D));
+    cfg.gridDim = dim3(static_cast<unsigned>((a.B * a.H + kCombineRows - 1) / kCombineRows));
+    cfg.blockDim = dim3(32 * kCombineRows);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = a.stream;
     cudaLaunchAttribute attr[1];
