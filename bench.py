@@ -350,6 +350,8 @@ def run_ours(args):
         return run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
     if args.only == "s-sweep":
         return run_s_sweep(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
+    if args.only == "prefill-configs":
+        return run_prefill_configs(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist)
     q, k, v, kv_len = wl.prefill_inputs(w, device=device, seed=w.seed + 1000 * rank)
     out = torch.empty_like(q)
 
@@ -497,6 +499,52 @@ def run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, ra
     return 0
 
 
+def run_prefill_configs(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
+    """The prefill workloads other than the headline one, each timed alone:
+    the small fp32 case (B2 H4 S128 D64, scale 1/8: too small for a
+    roofline, reported in microseconds), causal prefill with key padding
+    (B8 H16 S4096, lengths U{1024..4096}) and long-context causal prefill
+    (B1 H32 S16384).  FLOPs: the nominal count 4*B*H*S*S*D/2, and for the
+    padded batch the effective count sum_b 4*H*L_b*L_b*D/2 of the visible
+    (query, key) pairs, which is what the fraction of peak uses.  One JSON
+    line per workload; not part of the default run."""
+    names = [args.prefill_config] if args.prefill_config else ["tiny_f32", "padded", "long"]
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    for name in names:
+        w = wl.PREFILL_WORKLOADS[name]
+        q, k, v, kv_len = wl.prefill_inputs(w, device=device, seed=w.seed + 1000 * rank)
+        out = torch.empty_like(q)
+
+        def step():
+            attn.attn_fwd(q, k, v, out=out, scale=w.softmax_scale, causal=w.causal, kv_len=kv_len)
+
+        for _ in range(args.warmup):
+            step()
+        attn.attn_device_status()
+        ms = time_steps(step, args.steps, stream, flush)
+        attn.attn_device_status()
+        avg = max_over_ranks(dist, float(sum(ms)), device) / args.steps
+        nominal = prefill_flops(w.B, w.H, w.S, w.S, w.D, w.causal)
+        effective = nominal
+        if kv_len is not None:
+            lens = kv_len.cpu().tolist()
+            effective = float(sum(4.0 * w.H * float(L) * float(L) * w.D / (2.0 if w.causal else 1.0) for L in lens))
+        line = {"workload": w.name, "dtype": w.dtype, "ms_per_step": avg, "us_per_step": avg * 1e3,
+                "flops_nominal": nominal, "flops_effective": effective,
+                "TFLOP_per_s_nominal": nominal / (avg * 1e-3) / 1e12,
+                "TFLOP_per_s_effective": effective / (avg * 1e-3) / 1e12,
+                "kernel": "prefill_f32_kernel" if w.dtype == "f32" else f"prefill_tc_kernel<{w.D}>"}
+        if w.dtype != "f32":
+            line["frac_of_bf16_peak"] = line["TFLOP_per_s_effective"] / peak
+            line["peak"] = peak
+        if rank == 0:
+            print(json.dumps({"prefill_config": line}), flush=True)
+        del q, k, v, out
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def loglog_slope(xs, ys):
     """Least-squares slope of log(y) against log(x)."""
     lx, ly = np.log(np.asarray(xs, float)), np.log(np.asarray(ys, float))
@@ -620,9 +668,11 @@ def main():
                     help="approximate CPU time of the fp64 checker baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "decode-gqa", "s-sweep"],
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "decode-gqa", "s-sweep", "prefill-configs"],
                     default="all", help="profiling runs: time one kernel family only; s-sweep times "
-                    "prefill against sequence length")
+                    "prefill against sequence length; prefill-configs times the other prefill workloads")
+    ap.add_argument("--prefill-config", choices=["tiny_f32", "padded", "long"], default=None,
+                    help="prefill-configs runs: one workload only")
     ap.add_argument("--decode-batch", type=int, default=None,
                     help="profiling runs: smaller decode batch than the workload's 64")
     ap.add_argument("--decode-hkv", type=lambda x: [int(v) for v in x.split(",")], default=None,
