@@ -7,9 +7,10 @@
 // applied before the softmax); rows that see no key and padded query rows are
 // written as zeros.
 //
-// Work split: one CTA per (32 query rows, head, batch).  Four threads share a
-// query row, each holding every fourth element of q and of the output row in
-// registers; a score is a 4-way partial dot product summed with two lane
+// Work split: one CTA per (8 query rows, head, batch), so that even the small
+// fp32 workload (B2 H4 S128) spreads over 128 CTAs.  Sixteen threads share a
+// query row, each holding every sixteenth element of q and of the output row
+// in registers; a score is a 16-way partial dot product summed with four lane
 // shuffles.  K and V tiles of 32 keys are staged in shared memory.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -19,8 +20,8 @@
 namespace attn {
 namespace {
 
-constexpr int kRows = 32;         // query rows per CTA
-constexpr int kLanesPerRow = 4;   // threads sharing one query row
+constexpr int kRows = 8;          // query rows per CTA
+constexpr int kLanesPerRow = 16;  // threads sharing one query row
 constexpr int kThreads = kRows * kLanesPerRow;
 constexpr int kKeys = 32;         // keys per shared-memory tile
 constexpr float kLog2e = 1.4426950408889634f;
@@ -84,8 +85,8 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
             float part = 0.f;
 #pragma unroll
             for (int d = 0; d < DL; ++d) part = fmaf(q[d], ks[jj][d * kLanesPerRow + t], part);
-            part += __shfl_xor_sync(0xffffffffu, part, 1);
-            part += __shfl_xor_sync(0xffffffffu, part, 2);
+#pragma unroll
+            for (int o16 = 1; o16 < kLanesPerRow; o16 <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o16);
             s[jj] = (j0 + jj < lim) ? part * sl2 : -INFINITY;
             mt = fmaxf(mt, s[jj]);
         }
