@@ -274,7 +274,9 @@ def run_reference(args):
         return 0
     w = wl.PREFILL
     q, k, v, kv_len = wl.prefill_inputs(w, device="cpu")
-    per_step = max(2.0, min(10.0, 150.0 / max(args.steps + args.warmup, 1)))
+    # about 150 s of checker time for the whole run, whatever --steps is (each
+    # step a sample of at least 256 rows), at most 10 s a step
+    per_step = max(0.01, min(10.0, 150.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
         cpu_oracle_sample(q, k, v, w, kv_len, per_step / 4)
     vals, times, desc, threads = [], [], "", 0
