@@ -8,7 +8,14 @@ timed with CUDA events on the launching stream, L2 flushed between steps
 outside the events.  The decode workload (B64 H32 D128, cache padded to 8192,
 lengths uniform on [4096, 8192]) is timed the same way and reported under
 "decode".  "e2e" is the same prefill through attn_fwd_host from pinned host
-buffers, copies inside the timed call.  Rank 0 prints one JSON line.
+buffers, copies inside the timed call.  "configs" holds every workload --
+the fp32 one (B2 H4 S128 D64), the headline, causal + key padding (B8 H16
+S4096), long context (B1 H32 S16384) and decode -- each with its time, its
+roofline and the fp64 CPU oracle timed on the host cores (in full for the
+fp32, headline and decode workloads; on a seeded row sample, with an
+extrapolated full time, for the padded and long ones).  The line's
+`cpu_baseline` is the oracle over the whole headline workload.  Rank 0
+prints one JSON line.
 
 --impl reference times the fp64 CPU checker (the only reference this method
 has) on a bounded sample of the same workload, on the host cores.
@@ -111,7 +118,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every PERIOD_MS milliseconds."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -261,9 +268,95 @@ def cpu_oracle_sample(q, k, v, w, kv_len, budget_s, rng_seed=0):
     t0 = time.perf_counter()
     oracle.attention_rows(qc, kc, vc, rows, scale=w.softmax_scale, causal=w.causal, kv_len=kv_host)
     dt = time.perf_counter() - t0
-    desc = (f"{n} random query rows of the {w.name} workload ({flops / 1e9:.2f} GFLOP "
-            f"of the method's count), fp64, {dt:.1f} s")
+    desc = (f"{n} query rows of the {w.name} workload drawn uniformly with replacement "
+            f"({flops / 1e9:.2f} GFLOP of the method's count), fp64, {dt:.1f} s")
     return flops / dt / 1e12, desc, threads, dt
+
+
+def oracle_threads():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def visible_keys(w, kv_host, b, i):
+    """Keys query row i of sequence b sees (0 for a padded query row)."""
+    L = w.S if kv_host is None else int(kv_host[b])
+    if i >= L:
+        return 0
+    return min(i + 1, L) if w.causal else L
+
+
+def workload_flops(w, kv_host):
+    """The method's count, as the GPU legs use it: 4*B*H*S*S*D, halved for
+    causal; with key padding the effective count sum_b 4*H*L_b*L_b*D/2."""
+    if kv_host is None:
+        return prefill_flops(w.B, w.H, w.S, w.S, w.D, w.causal)
+    return float(sum(4.0 * w.H * float(L) * float(L) * w.D / (2.0 if w.causal else 1.0) for L in kv_host))
+
+
+def cpu_oracle_full(q, k, v, w, kv_len, repeat=1):
+    """The fp64 oracle over the whole workload (every output row), timed on
+    the host cores; the fastest of `repeat` runs."""
+    import oracle
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    kv_host = None if kv_len is None else kv_len.cpu().numpy()
+    best = None
+    for _ in range(repeat):
+        t0 = time.perf_counter()
+        oracle.attention(qc, kc, vc, scale=w.softmax_scale, causal=w.causal, kv_len=kv_host)
+        dt = time.perf_counter() - t0
+        best = dt if best is None else min(best, dt)
+    flops = workload_flops(w, kv_host)
+    rows = w.B * w.H * w.S
+    return {"value": flops / best / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"the whole {w.name} workload: all {rows} output rows, fp64, {best:.3f} s"
+                      + (f" (fastest of {repeat} runs)" if repeat > 1 else ""),
+            "seconds": best, "rows_per_s": rows / best, "extrapolated": False}
+
+
+def cpu_oracle_rows_sample(q, k, v, w, kv_len, seed):
+    """The fp64 oracle on a seeded row sample: for every (b, h) the rows 0, 1,
+    127, 128, L_b - 1, L_b and S - 1, plus 64 rows drawn without replacement.
+    Reports the sample's TFLOP/s and rows/s, and a full-workload time
+    extrapolated from the sample by the method's flop count."""
+    import oracle
+    kv_host = None if kv_len is None else kv_len.cpu().numpy()
+    rng = np.random.default_rng(seed)
+    rows = []
+    for b in range(w.B):
+        L = w.S if kv_host is None else int(kv_host[b])
+        fixed = {0, 1, 127, 128, L - 1, L, w.S - 1}
+        for h in range(w.H):
+            pick = {i for i in fixed if 0 <= i < w.S} | set(rng.choice(w.S, 64, replace=False).tolist())
+            rows += [(b, h, i) for i in sorted(pick)]
+    rows = np.array(rows, dtype=np.int64)
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    t0 = time.perf_counter()
+    oracle.attention_rows(qc, kc, vc, rows, scale=w.softmax_scale, causal=w.causal, kv_len=kv_host)
+    dt = time.perf_counter() - t0
+    sample_flops = float(sum(4.0 * w.D * visible_keys(w, kv_host, int(b), int(i)) for b, _, i in rows))
+    exact_flops = float(sum(4.0 * w.D * visible_keys(w, kv_host, b, i) for b in range(w.B) for i in range(w.S)) * w.H)
+    rate = sample_flops / dt
+    return {"value": rate / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": (f"{len(rows)} query rows of the {w.name} workload (per (b, h): rows 0, 1, 127, 128, "
+                       f"L-1, L, S-1 and 64 drawn without replacement, seed {seed}), fp64, {dt:.2f} s"),
+            "seconds": dt, "rows": int(len(rows)), "rows_per_s": len(rows) / dt,
+            "extrapolated": True, "extrapolated_full_seconds": exact_flops / rate}
+
+
+def cpu_oracle_decode(q, kc, vc, kv_len, dwk):
+    """The fp64 oracle over the whole decode workload (every (b, h) row),
+    reported as GB/s of the K/V bytes the method reads and as TFLOP/s."""
+    import oracle
+    lens = kv_len.cpu().numpy()
+    qh, kh, vh = q.cpu(), kc.cpu(), vc.cpu()
+    t0 = time.perf_counter()
+    oracle.decode(qh, kh, vh, kv_len=lens)
+    dt = time.perf_counter() - t0
+    nbytes = decode_bytes(dwk.H, dwk.D, lens.tolist())
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"the whole {dwk.name} workload: all {dwk.B * dwk.H} query rows, fp64, {dt:.3f} s",
+            "seconds": dt, "tflops": decode_flops(dwk.H, dwk.D, lens.tolist()) / dt / 1e12,
+            "extrapolated": False}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -393,13 +486,21 @@ def run_ours(args):
                 "algorithmic_flops_per_launch": flops_step}
 
     # -------------------------------------------------------------- decode
-    decode = None if args.only == "prefill" else decode_leg(args, attn, device, stream, flush, peaks,
-                                                            peak_src, world, rank, dist)
+    decode, decode_tensors = (None, None) if args.only == "prefill" else decode_leg(
+        args, attn, device, stream, flush, peaks, peak_src, world, rank, dist, keep=True)
     e2e = None if args.no_e2e else e2e_leg(args, attn, q, k, v, out, w, flops_step, world, dist, device)
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, desc, threads, _ = cpu_oracle_sample(q, k, v, w, kv_len, args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+    cpu_on = rank == 0 and world == 1 and not args.no_cpu_baseline
+    cpu = cpu_oracle_full(q, k, v, w, kv_len) if cpu_on else None
+    configs = None
+    if args.only == "all" and not args.no_configs:
+        configs = config_legs(args, attn, device, stream, flush, peaks, world, rank, dist, cpu_on)
+        configs["prefill"] = {"workload": w.name, "seed": w.seed + 1000 * rank, "ms_per_step": avg_ms,
+                              "TFLOP_per_s": achieved, "roofline": roofline, "cpu_baseline": cpu,
+                              "note": "the headline workload: the line's own value"}
+        if decode is not None:
+            configs["decode"] = dict(decode)
+            if cpu_on:
+                configs["decode"]["cpu_baseline"] = cpu_oracle_decode(*decode_tensors, wl.DECODE)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -407,7 +508,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16)",
         "config": config_dict(w, world),
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode, "configs": configs,
         "clocks": clocks, "gpu_launches": args.steps,
         "wall_s_timed_region": wall, "kernel_source_digest": kernel_source_digest(),
         "env": run_env(device, {"prefill": w.seed, "decode": wl.DECODE.seed, "rank_offset": 1000}),
@@ -419,7 +520,26 @@ def run_ours(args):
     return 0
 
 
-def decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
+def config_legs(args, attn, device, stream, flush, peaks, world, rank, dist, cpu_on):
+    """The other workloads beside the headline one, each with its own time,
+    roofline and fp64 oracle baseline: the fp32 workload (oracle run in
+    full), the padded and the long-context workloads (oracle on a seeded row
+    sample, with a full time extrapolated from it)."""
+    out = {}
+    for name in ("tiny_f32", "padded", "long"):
+        line, (q, k, v, kv_len) = prefill_workload_leg(name, args, attn, device, stream, flush, peaks,
+                                                       world, rank, dist)
+        if cpu_on:
+            w = wl.PREFILL_WORKLOADS[name]
+            line["cpu_baseline"] = (cpu_oracle_full(q, k, v, w, kv_len, repeat=5) if name == "tiny_f32"
+                                    else cpu_oracle_rows_sample(q, k, v, w, kv_len, seed=w.seed))
+        out[name] = line
+        del q, k, v, kv_len
+        torch.cuda.empty_cache()
+    return out
+
+
+def decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist, keep=False):
     dwk = wl.DECODE
     if args.decode_batch:
         dwk = wl.DecodeWorkload(dwk.name.replace("B64", f"B{args.decode_batch}"), args.decode_batch,
@@ -441,7 +561,8 @@ def decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, 
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     d_gbs = dbytes / (d_avg * 1e-3) / 1e9
     decode = {
-        "workload": dwk.name, "value": world * dbytes * args.steps / (dtotal * 1e-3) / 1e9,
+        "workload": dwk.name, "seed": dwk.seed + 1000 * rank,
+        "value": world * dbytes * args.steps / (dtotal * 1e-3) / 1e9,
         "unit": "GB/s", "ms_per_step": d_avg,
         "tflops": decode_flops(dwk.H, dwk.D, dkl.cpu().tolist()) / (d_avg * 1e-3) / 1e12,
         "splits_per_head": attn.attn_decode_splits(dwk.B, dwk.H, dwk.Skv, dwk.D),
@@ -453,6 +574,8 @@ def decode_leg(args, attn, device, stream, flush, peaks, peak_src, world, rank, 
                      "peak_source": f"{peak_src} HBM copy bandwidth",
                      "algorithmic_bytes_per_launch": dbytes},
     }
+    if keep:
+        return decode, (dq, dk, dv, dkl)
     del dq, dk, dv, dout
     return decode
 
@@ -501,47 +624,62 @@ def run_decode_gqa(args, attn, device, stream, flush, peaks, peak_src, world, ra
     return 0
 
 
+PROFILE_SUMMARIES = {"prefill": "prefill_tc_B4H32S2048D128.md", "padded": "prefill_tc_padded_B8H16S4096D128.md",
+                     "long": "prefill_tc_long_B1H32S16384D128.md", "tiny_f32": "prefill_f32_B2H4S128D64.md"}
+
+
+def prefill_workload_leg(name, args, attn, device, stream, flush, peaks, world, rank, dist):
+    """Time one prefill workload alone (CUDA events, L2 flushed between calls).
+    Returns (line, (q, k, v, kv_len)).  FLOPs: the nominal count
+    4*B*H*S*S*D/2 and, with key padding, the effective count
+    sum_b 4*H*L_b*L_b*D/2 of the visible (query, key) pairs, which the
+    fraction of peak uses.  The fp32 workload is latency-bound (16.8 MFLOP):
+    it has no roofline, its figure is the time per call."""
+    w = wl.PREFILL_WORKLOADS[name]
+    q, k, v, kv_len = wl.prefill_inputs(w, device=device, seed=w.seed + 1000 * rank)
+    out = torch.empty_like(q)
+
+    def step():
+        attn.attn_fwd(q, k, v, out=out, scale=w.softmax_scale, causal=w.causal, kv_len=kv_len)
+
+    for _ in range(args.warmup):
+        step()
+    attn.attn_device_status()
+    ms = time_steps(step, args.steps, stream, flush)
+    attn.attn_device_status()
+    avg = max_over_ranks(dist, float(sum(ms)), device) / args.steps
+    nominal = prefill_flops(w.B, w.H, w.S, w.S, w.D, w.causal)
+    effective = workload_flops(w, None if kv_len is None else kv_len.cpu().numpy())
+    kernel = "prefill_f32_kernel" if w.dtype == "f32" else f"prefill_tc_kernel<{w.D}>"
+    line = {"workload": w.name, "dtype": w.dtype, "seed": w.seed + 1000 * rank, "steps": args.steps,
+            "ms_per_step": avg, "us_per_step": avg * 1e3,
+            "flops_nominal": nominal, "flops_effective": effective,
+            "TFLOP_per_s_nominal": nominal / (avg * 1e-3) / 1e12,
+            "TFLOP_per_s_effective": effective / (avg * 1e-3) / 1e12,
+            "kernel": kernel, "gpu_launches": args.steps}
+    if w.dtype == "f32":
+        line["roofline"] = {"bound": "latency", "note": "16.8 MFLOP per call: too small to fill the GPU; "
+                            "the figure is the time per call"}
+    else:
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        achieved = line["TFLOP_per_s_effective"]
+        line["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                            "frac": achieved / peak,
+                            "traffic": profiled_traffic(PROFILE_SUMMARIES[name], "prefill_tc.cu"),
+                            "kernel": kernel, "algorithmic_flops_per_launch": effective}
+    return line, (q, k, v, kv_len)
+
+
 def run_prefill_configs(args, attn, device, stream, flush, peaks, peak_src, world, rank, dist):
-    """The prefill workloads other than the headline one, each timed alone:
-    the small fp32 case (B2 H4 S128 D64, scale 1/8: too small for a
-    roofline, reported in microseconds), causal prefill with key padding
-    (B8 H16 S4096, lengths U{1024..4096}) and long-context causal prefill
-    (B1 H32 S16384).  FLOPs: the nominal count 4*B*H*S*S*D/2, and for the
-    padded batch the effective count sum_b 4*H*L_b*L_b*D/2 of the visible
-    (query, key) pairs, which is what the fraction of peak uses.  One JSON
-    line per workload; not part of the default run."""
+    """The prefill workloads other than the headline one, each timed alone
+    (see prefill_workload_leg).  One JSON line per workload; not part of the
+    default run."""
     names = [args.prefill_config] if args.prefill_config else ["tiny_f32", "padded", "long"]
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     for name in names:
-        w = wl.PREFILL_WORKLOADS[name]
-        q, k, v, kv_len = wl.prefill_inputs(w, device=device, seed=w.seed + 1000 * rank)
-        out = torch.empty_like(q)
-
-        def step():
-            attn.attn_fwd(q, k, v, out=out, scale=w.softmax_scale, causal=w.causal, kv_len=kv_len)
-
-        for _ in range(args.warmup):
-            step()
-        attn.attn_device_status()
-        ms = time_steps(step, args.steps, stream, flush)
-        attn.attn_device_status()
-        avg = max_over_ranks(dist, float(sum(ms)), device) / args.steps
-        nominal = prefill_flops(w.B, w.H, w.S, w.S, w.D, w.causal)
-        effective = nominal
-        if kv_len is not None:
-            lens = kv_len.cpu().tolist()
-            effective = float(sum(4.0 * w.H * float(L) * float(L) * w.D / (2.0 if w.causal else 1.0) for L in lens))
-        line = {"workload": w.name, "dtype": w.dtype, "ms_per_step": avg, "us_per_step": avg * 1e3,
-                "flops_nominal": nominal, "flops_effective": effective,
-                "TFLOP_per_s_nominal": nominal / (avg * 1e-3) / 1e12,
-                "TFLOP_per_s_effective": effective / (avg * 1e-3) / 1e12,
-                "kernel": "prefill_f32_kernel" if w.dtype == "f32" else f"prefill_tc_kernel<{w.D}>"}
-        if w.dtype != "f32":
-            line["frac_of_bf16_peak"] = line["TFLOP_per_s_effective"] / peak
-            line["peak"] = peak
+        line, tensors = prefill_workload_leg(name, args, attn, device, stream, flush, peaks, world, rank, dist)
         if rank == 0:
             print(json.dumps({"prefill_config": line}), flush=True)
-        del q, k, v, out
+        del tensors
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -666,10 +804,10 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="approximate CPU time of the fp64 checker baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (fp32, padded, long context) in the default line")
     ap.add_argument("--only", choices=["all", "prefill", "decode", "decode-gqa", "s-sweep", "prefill-configs"],
                     default="all", help="profiling runs: time one kernel family only; s-sweep times "
                     "prefill against sequence length; prefill-configs times the other prefill workloads")

@@ -67,6 +67,7 @@ extern "C" {
 #define ATTN_ECUDA (-3)        /* a CUDA runtime or driver call failed; see attn_last_error() */
 #define ATTN_ENOMEM (-4)       /* workspace allocation failed */
 #define ATTN_ETIMEOUT (-5)     /* a device-side wait hit its iteration limit (reported by attn_device_status) */
+#define ATTN_ECONFLICT (-6)    /* two bf16 prefill launches shared one work counter (reported by attn_device_status) */
 
 /*
  * attn_fwd -- prefill attention for a batch of multi-head sequences.
@@ -96,6 +97,19 @@ extern "C" {
  *
  * Sizes: B, H >= 1; Sq, Skv >= 0 (an empty call returns ATTN_OK and does
  * nothing); D as above; B*H*max(Sq,Skv)*D must fit in 2^31 rows of D.
+ *
+ * Concurrency (bf16).  The kernel hands out its work through a counter in a
+ * fixed table of the library (no allocation, no clearing launch).  Direct
+ * calls take the table's first 64 counters in turn, so at most 64 bf16
+ * prefill calls (attn_fwd, attn_fwd_gqa, attn_fwd_chunked, attn_fwd_host's
+ * chunks) may be in flight on one device at once.  A call made while its
+ * stream is being captured into a CUDA graph gets a counter of its own from
+ * 1024 further ones, which every replay of that graph node uses; so one
+ * graph must not be replayed on two streams at the same time, and at most
+ * 1024 captured prefill calls should be alive.  A launch that finds its
+ * counter in use by another launch records that in the device status word:
+ * attn_device_status() then returns ATTN_ECONFLICT, and the outputs of both
+ * launches are undefined.
  */
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
                       int Sq, int Skv, int D, float scale, int causal, const int32_t *kv_len,
@@ -234,6 +248,14 @@ ATTN_API int attn_fwd_debug(const void *q, const void *k, const void *v, void *o
  * the library allocates on first use (and grows when a call needs more),
  * which attn_release() frees.  The workspace is shared by all calls on a
  * device: calls that overlap in time on different streams of one device race.
+ *
+ * CUDA graphs: a captured call keeps the workspace's address.  Growing the
+ * workspace never frees the old buffer (it is kept until attn_release), so
+ * a graph captured before a larger call stays valid.  A call made during a
+ * capture cannot allocate: if it needs a larger workspace than the device
+ * has, it returns ATTN_EINVAL without enqueuing anything, so make one
+ * ordinary call of the largest size before capturing.  Destroy every graph
+ * that holds a decode call before attn_release().
  */
 ATTN_API int attn_decode(const void *q, const void *kcache, const void *vcache, void *out, int B,
                          int H, int Skv, int D, const int32_t *kv_len, int dtype, void *stream);
@@ -303,7 +325,9 @@ ATTN_API int attn_decode_splits(int B, int H, int Skv, int D);
 /*
  * attn_device_status -- synchronise `stream`, then report and clear the
  * device-side status word.  Returns ATTN_OK, ATTN_ETIMEOUT when a kernel gave
- * up on a device-side wait (its output is then undefined), or ATTN_ECUDA when
+ * up on a device-side wait (its output is then undefined), ATTN_ECONFLICT
+ * when two bf16 prefill launches in flight shared one work counter (see
+ * attn_fwd, "Concurrency"; both outputs are undefined), or ATTN_ECUDA when
  * the synchronisation itself failed.
  */
 ATTN_API int attn_device_status(void *stream);
@@ -324,8 +348,9 @@ ATTN_API int attn_selftest_wait_timeout(long long limit_cycles, void *stream);
 ATTN_API const char *attn_last_error(void);
 
 /* Free library-owned device memory on the current device: the decode
- * workspace and attn_fwd_host's device copies.  Not while a call that uses
- * them is running. */
+ * workspace (with every smaller buffer it replaced) and attn_fwd_host's
+ * device copies.  Not while a call that uses them is running, and not while
+ * a CUDA graph that holds a decode call may still be replayed. */
 ATTN_API void attn_release(void);
 
 #ifdef __cplusplus

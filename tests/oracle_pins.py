@@ -354,6 +354,33 @@ def pin_lse_is_log_sum_exp(att):
                     assert lse[b, h, i] == -np.inf
 
 
+def pin_lengths_outside_range_are_clamped(att):
+    """Length entries outside [0, Skv] act as the nearest end of the range.  A
+    length above the capacity makes every key valid, so prefill equals the
+    unpadded call and a chunk against its cache equals the last Sq rows of full
+    causal attention over all Skv keys, checked against PyTorch's float64
+    scaled_dot_product_attention ('Attention from scratch'
+    (open-llm-engineering), "KV cache position drift": positions are absolute).
+    A negative length leaves no visible key, so the row is zero (the library's
+    rule for a row the pages treat as an error)."""
+    B, H, S, D, Sq = 2, 2, 7, 4, 3
+    q, k, v = _rand((B, H, S, D), 130), _rand((B, H, S, D), 131), _rand((B, H, S, D), 132)
+    scale = 1.0 / math.sqrt(D)
+    ii, jj = np.arange(S)[:, None], np.arange(S)[None, :]
+    ref = _torch_sdpa_f64(q, k, v, np.broadcast_to((jj <= ii)[None, None], (B, 1, S, S)), scale)
+    out = att(q, k, v, scale=scale, causal=True, kv_len=np.array([S + 5, -3], np.int32))
+    np.testing.assert_allclose(out[0], ref[0], rtol=0, atol=1e-12)
+    assert np.all(out[1] == 0.0)
+    qc = np.ascontiguousarray(q[:, :, S - Sq:])
+    out_c = att(qc, k, v, scale=scale, causal=True, cache_len=np.array([S + 9, -2], np.int32))
+    np.testing.assert_allclose(out_c[0], ref[0, :, S - Sq:], rtol=0, atol=1e-12)
+    assert np.all(out_c[1] == 0.0)
+    dec = att(q[:, :, S - 1:], k, v, scale=scale, causal=False,
+              kv_len=np.array([S + 1, -7], np.int32), query_padding=False)
+    np.testing.assert_allclose(dec[0, :, 0], ref[0, :, S - 1], rtol=0, atol=1e-12)
+    assert np.all(dec[1] == 0.0)
+
+
 ALL_PINS = [
     pin_tiny_example_causal,
     pin_kube_dojo_example,
@@ -372,4 +399,5 @@ ALL_PINS = [
     pin_grouped_query_matches_library,
     pin_cache_chunk_is_tail_of_full_causal,
     pin_lse_is_log_sum_exp,
+    pin_lengths_outside_range_are_clamped,
 ]

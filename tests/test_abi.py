@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(attn_lib):
 def test_status_codes_match_header():
     text = open(HEADER).read()
     for name in ("ATTN_OK", "ATTN_EINVAL", "ATTN_EUNSUPPORTED", "ATTN_ECUDA", "ATTN_ENOMEM",
-                 "ATTN_ETIMEOUT", "ATTN_F32", "ATTN_BF16"):
+                 "ATTN_ETIMEOUT", "ATTN_ECONFLICT", "ATTN_F32", "ATTN_BF16"):
         m = re.search(rf"#define\s+{name}\s+\(?(-?\d+)\)?", text)
         assert m, name
         assert int(m.group(1)) == getattr(attn, name)

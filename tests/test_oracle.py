@@ -86,6 +86,7 @@ MUTANTS = {
     "lse_without_max": ("*lse = m + log(z);", "*lse = log(z);"),
     "cache_offset_from_capacity": ("Lb - Sq, Skv, Dk, Dv, scale, 1, Lb, 0,", "Skv - Sq, Skv, Dk, Dv, scale, 1, Lb, 0,"),
     "kv_head_by_modulo": ("size_t pkv = (size_t)b * Hkv + h / G;", "size_t pkv = (size_t)b * Hkv + h % Hkv;"),
+    "length_clamp_dropped": ("    if (L < 0)\n        L = 0;\n    if (L > Skv)\n        L = Skv;\n", ""),
     "keys_from_query_row": ("load_elem(k, dtype, k_bh + (size_t)j * Dk + d)",
                             "load_elem(k, dtype, k_bh + (size_t)j * Dk + d) * 0.0 + "
                             "load_elem(q, dtype, q_bh + (size_t)i * Dk + d)"),

@@ -24,6 +24,7 @@ ATTN_EUNSUPPORTED = -2
 ATTN_ECUDA = -3
 ATTN_ENOMEM = -4
 ATTN_ETIMEOUT = -5
+ATTN_ECONFLICT = -6
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn.so")
@@ -326,7 +327,8 @@ def attn_decode_splits(B: int, H: int, Skv: int, D: int) -> int:
 
 
 def attn_device_status(stream=None) -> None:
-    """Synchronise the stream and raise AttnError if a kernel reported a timeout."""
+    """Synchronise the stream and raise AttnError if a kernel reported a timed-out
+    wait (ATTN_ETIMEOUT) or a shared prefill work counter (ATTN_ECONFLICT)."""
     _check(lib().attn_device_status(_stream_handle(stream)))
 
 
@@ -343,5 +345,5 @@ __all__ = [
     "attn_fwd", "attn_fwd_chunked", "attn_fwd_debug", "attn_fwd_host", "attn_decode", "attn_decode_noalloc", "attn_decode_splits", "attn_device_status", "attn_release",
     "attn_last_error", "attn_selftest_wait_timeout", "lib", "AttnError", "SIGNATURES", "LIB_PATH",
     "ATTN_F32", "ATTN_BF16", "ATTN_OK", "ATTN_EINVAL", "ATTN_EUNSUPPORTED", "ATTN_ECUDA",
-    "ATTN_ENOMEM", "ATTN_ETIMEOUT",
+    "ATTN_ENOMEM", "ATTN_ETIMEOUT", "ATTN_ECONFLICT",
 ]

@@ -146,28 +146,44 @@ int make_map_rows(CUtensorMap *map, const void *base, int D, long long rows) {
 
 // ------------------------------------------------------------ decode workspace
 
+// The decode partials.  A buffer the workspace outgrows is kept on the
+// retired list, not freed: a CUDA graph captured earlier may still write to
+// it on every replay.  attn_release frees them all.
+constexpr int kMaxRetired = 64;
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
+    void *retired[kMaxRetired] = {};
+    int n_retired = 0;
 };
 Workspace g_ws[kMaxDevices];
 
-int workspace(size_t bytes, void **out) {
+int workspace(size_t bytes, cudaStream_t stream, void **out) {
     int dev;
     int rc = current_device(&dev);
     if (rc) return rc;
     std::lock_guard<std::mutex> lock(g_mutex);
     Workspace &w = g_ws[dev];
     if (w.bytes < bytes) {
-        if (w.ptr) cudaFree(w.ptr);  // synchronises the device: no call still uses it
-        w.ptr = nullptr;
-        w.bytes = 0;
-        cudaError_t e = cudaMalloc(&w.ptr, bytes);
-        if (e != cudaSuccess) {
-            w.ptr = nullptr;
-            return fail(ATTN_ENOMEM, "decode workspace of %zu bytes: %s", bytes, cudaGetErrorString(e));
-        }
-        w.bytes = bytes;
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+        if (cap != cudaStreamCaptureStatusNone)
+            return fail(ATTN_EINVAL,
+                        "attn_decode: a captured call needs %zu bytes of workspace but the device has %zu; "
+                        "make one ordinary call of this size before capturing",
+                        bytes, w.bytes);
+        if (w.ptr && w.n_retired == kMaxRetired)
+            return fail(ATTN_ENOMEM, "attn_decode: the workspace grew %d times; call attn_release", kMaxRetired);
+        // grow at least geometrically, so retired buffers add up to less than the live one
+        const size_t want = bytes > 2 * w.bytes ? bytes : 2 * w.bytes;
+        void *p = nullptr;
+        e = cudaMalloc(&p, want);
+        if (e != cudaSuccess)
+            return fail(ATTN_ENOMEM, "decode workspace of %zu bytes: %s", want, cudaGetErrorString(e));
+        if (w.ptr) w.retired[w.n_retired++] = w.ptr;
+        w.ptr = p;
+        w.bytes = want;
     }
     *out = w.ptr;
     return ATTN_OK;
@@ -532,7 +548,7 @@ ATTN_API int attn_decode_gqa(const void *q, const void *kcache, const void *vcac
     const size_t o_bytes = static_cast<size_t>(bh) * n_split * D * sizeof(float);
     const size_t ml_bytes = static_cast<size_t>(bh) * n_split * 2 * sizeof(float);
     void *ws = nullptr;
-    int rc = workspace(o_bytes + ml_bytes, &ws);
+    int rc = workspace(o_bytes + ml_bytes, static_cast<cudaStream_t>(stream), &ws);
     if (rc) return rc;
     int *status = nullptr;
     if ((rc = status_word(&status))) return rc;
@@ -611,6 +627,10 @@ ATTN_API int attn_device_status(void *stream) {
     const int zero = 0;
     e = cudaMemcpy(status, &zero, sizeof zero, cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "attn_device_status: clear status word");
+    if ((word & 0xff) == kStatusSchedConflict)
+        return fail(ATTN_ECONFLICT,
+                    "two bf16 prefill launches in flight shared one work counter (site 0x%x); "
+                    "their outputs are undefined", word >> 8);
     return fail(ATTN_ETIMEOUT, "a device-side wait gave up (site 0x%x); that call's output is undefined",
                 word >> 8);
 }
@@ -631,9 +651,12 @@ ATTN_API void attn_release(void) {
     if (current_device(&dev)) return;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (g_ws[dev].ptr) cudaFree(g_ws[dev].ptr);
-        g_ws[dev].ptr = nullptr;
-        g_ws[dev].bytes = 0;
+        Workspace &w = g_ws[dev];
+        if (w.ptr) cudaFree(w.ptr);
+        for (int i = 0; i < w.n_retired; ++i) cudaFree(w.retired[i]);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        w.n_retired = 0;
     }
     // outside g_mutex: attn_fwd_host takes its own lock first, then g_mutex
     g_host[dev].release();

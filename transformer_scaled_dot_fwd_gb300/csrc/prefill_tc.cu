@@ -63,7 +63,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
 constexpr int kItemRing = 4;          // work items in flight between the roles
 constexpr int kItemReaders = 32 + 256;  // MMA warp + both softmax warpgroups
-constexpr int kSchedSlots = 64;       // launches that may run at once with their own counter
+constexpr int kSchedSlots = 64;       // direct launches that may run at once with their own counter
+constexpr int kGraphSlots = 1024;     // counters kept for launches captured into CUDA graphs
 // Bytes of keys and values per block of heads in the item order (see
 // decode_item); 0 puts all heads in one block.
 #ifndef ATTN_L2_GROUP_MB
@@ -109,7 +110,6 @@ struct Item {
 };
 
 struct Bars {
-    long long t0;  // CTA start clock (timeline probes)
     uint64_t q_full[2];
     uint64_t q_empty[2];
     uint64_t kv_full[8];
@@ -126,55 +126,15 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-// Work counters, one pair per launch slot: [0] next item, [1] CTAs finished.
-// The last CTA of a launch resets both, so the next launch on the slot starts
-// from zero without a separate clearing step.
-__device__ unsigned int g_sched[kSchedSlots][2];
-
-// Timeline probes for profiling builds (compiled out unless ATTN_TRACE is
-// defined): in chosen CTAs, the TMA thread, the MMA warp and one thread of
-// each softmax warpgroup record (event, SM clock since CTA start) straight to
-// global memory; each CTA can also log its SM, start, MMA-done and end times.
-#ifdef ATTN_TRACE
-constexpr int kTraceRoles = 4, kTraceEvents = 2048;
-__device__ long long *g_trace_buf;
-__device__ int g_trace_ctas[4];
-__device__ unsigned long long *g_cta_log;
-extern "C" __attribute__((visibility("default"))) int attn_trace_set(long long *buf, const int *ctas) {
-    cudaMemcpyToSymbol(g_trace_buf, &buf, sizeof buf);
-    return static_cast<int>(cudaMemcpyToSymbol(g_trace_ctas, ctas, 4 * sizeof(int)));
-}
-extern "C" __attribute__((visibility("default"))) int attn_cta_log_set(unsigned long long *buf) {
-    return static_cast<int>(cudaMemcpyToSymbol(g_cta_log, &buf, sizeof buf));
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ unsigned sm_id() {
-    unsigned s;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
-    return s;
-}
-#define CTA_LOG(slot)                                                               \
-    if (g_cta_log) g_cta_log[static_cast<size_t>(blockIdx.x) * 4 + (slot)] = (slot) == 0 ? sm_id() : global_ns();
-#define TRACE_SETUP(t0_smem)                                                        \
-    int trace_slot = -1, trace_n = 0;                                               \
-    for (int ts = 0; ts < 4; ++ts)                                                  \
-        if (g_trace_ctas[ts] == static_cast<int>(blockIdx.x) && g_trace_buf) trace_slot = ts; \
-    if (threadIdx.x == 0) { t0_smem = clock64(); CTA_LOG(0) CTA_LOG(1) }
-#define TRACE(role, code, t0)                                                       \
-    do {                                                                            \
-        if (trace_slot >= 0 && trace_n < kTraceEvents)                              \
-            g_trace_buf[(trace_slot * kTraceRoles + (role)) * kTraceEvents + trace_n++] = \
-                (static_cast<long long>(code) << 40) | (clock64() - (t0));          \
-    } while (0)
-#else
-#define TRACE_SETUP(t0_smem)
-#define TRACE(role, code, t0)
-#define CTA_LOG(slot)
-#endif
+// Work counters, one slot per launch: [0] next item, [1] CTAs finished,
+// [2] epoch of the launch using the slot (0: free).  The last CTA of a launch
+// resets all three, so the next launch on the slot starts from zero without a
+// separate clearing step.  Direct launches take slots [0, kSchedSlots) in
+// turn; a launch captured into a CUDA graph gets its own slot from the
+// kGraphSlots after them, so replays never share a counter with direct
+// launches.  A CTA that finds another launch's epoch in its slot reports
+// kStatusSchedConflict: the two launches' outputs are then undefined.
+__device__ unsigned int g_sched[kSchedSlots + kGraphSlots][4];
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
@@ -298,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tq,
                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                       const int n_major, const int group, const int front, const int n_items,
-                      unsigned int *sched) {
+                      unsigned int *sched, const unsigned int epoch) {
     using L = Layout<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -307,7 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars &bars = *reinterpret_cast<Bars *>(smem + L::kBarOff);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    TRACE_SETUP(bars.t0)
 
     if (threadIdx.x == 0) {
         for (int x = 0; x < kQTiles; ++x) {
@@ -328,6 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars.mma_done, 1);
         bars.abort = 0;
         fence_mbar_init();
+        // claim the slot for this launch (the first CTA finds it free, the
+        // others find this launch's epoch)
+        const unsigned int owner = atomicExch(sched + 2, epoch);
+        if (owner != 0u && owner != epoch) report_status(a.status, 0x12, kStatusSchedConflict);
     }
     if (warp == 1) {
         tmem_alloc(&bars.tmem_base, kTmemCols);
@@ -364,7 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 publish_item(bars, slot, it);
                 mbar_arrive(&bars.item_full[slot]);
                 if (it.N < 0) break;
-                TRACE(0, 400 + (k % 100) * 100000, bars.t0);
                 // ---- loads in the order the MMA warp consumes them: Q_0, K_0,
                 // Q_1, V_0, K_1, V_1, ...  (Q_1 waits for the previous item's
                 // last S1 to free its buffer; K_0 need not wait for that).
@@ -387,7 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (issued >= L::kStages &&
                         !(ok = mbar_wait(&bars.kv_empty[s], ((issued / L::kStages) - 1) & 1, &bars.abort)))
                         return;
-                    TRACE(0, 300 + kv + j * 1000 + (k % 100) * 100000, bars.t0);
                     mbar_arrive_expect_tx(&bars.kv_full[s], L::kTileBytes);
 #pragma unroll
                     for (int c = 0; c < L::kSub; ++c)
@@ -440,7 +401,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t q_uses[kQTiles] = {0, 0}, pr[kQTiles] = {0, 0};
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            TRACE(1, 109 + (k % 100) * 100000, bars.t0);
             Item it;
             if (!(ok = take_item(bars, k, &it))) break;
             release_item(bars, k);
@@ -453,7 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int N = it.N;
             if (N < 0) break;
             if (N == 0) continue;
-            TRACE(1, 110 + (k % 100) * 100000, bars.t0);
             // S_x_0 per query tile as soon as Q_x and K_0 are in (Q_1 may land
             // after Q_0: the previous item's last S1 freed its buffer late)
             {
@@ -463,7 +422,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int x = 0; x < kQTiles; ++x) {
                     if (it.n_kv[x] == 0) continue;
                     if (!(ok = mbar_wait_warp(&bars.q_full[x], q_uses[x] & 1, &bars.abort))) break;
-                    TRACE(1, 111 + 2 * x + (k % 100) * 100000, bars.t0);
                     ++q_uses[x];
                     if (!have_k) {
                         kslot = consumed % L::kStages;
@@ -474,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     issue_s(x, kslot);
-                    TRACE(1, 112 + 2 * x + (k % 100) * 100000, bars.t0);
                     tc_commit_warp(&bars.s_full[x]);
                     if (it.n_kv[x] == 1) tc_commit_warp(&bars.q_empty[x]);  // last read of Q_x
                 }
@@ -482,19 +439,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_warp(&bars.kv_empty[kslot]);
             }
             for (int j = 0; j < N && ok; ++j) {
-                TRACE(1, 100 + j * 1000 + (k % 100) * 100000, bars.t0);
                 const int vslot = consumed % L::kStages;
                 if (!(ok = mbar_wait_warp(&bars.kv_full[vslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                 ++consumed;
                 tc_fence_after();
-                TRACE(1, 101 + j * 1000 + (k % 100) * 100000, bars.t0);
                 if (j < it.n_kv[0]) {
                     if (!(ok = mbar_wait_warp(&bars.p_ready[0], pr[0], &bars.abort))) break;
-                    TRACE(1, 102 + j * 1000 + (k % 100) * 100000, bars.t0);
                     pr[0] ^= 1;
                     tc_fence_after();
                     issue_pv(0, vslot, j > 0);
-                    TRACE(1, 105 + j * 1000 + (k % 100) * 100000, bars.t0);
                     if (j == it.n_kv[0] - 1) tc_commit_warp(&bars.o_full[0]);
                 }
                 const bool next = j + 1 < N;
@@ -504,28 +457,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait_warp(&bars.kv_full[nslot], (consumed / L::kStages) & 1, &bars.abort))) break;
                     ++consumed;
                     tc_fence_after();
-                    TRACE(1, 108 + j * 1000 + (k % 100) * 100000, bars.t0);
                     if (j + 1 < it.n_kv[0]) {
                         issue_s(0, nslot);  // overwrites P0_j: PV0_j was issued first
                         tc_commit_warp(&bars.s_full[0]);
                         if (j + 2 == it.n_kv[0]) tc_commit_warp(&bars.q_empty[0]);
                     }
                 }
-                TRACE(1, 103 + j * 1000 + (k % 100) * 100000, bars.t0);
                 if (j < it.n_kv[1]) {
                     if (!(ok = mbar_wait_warp(&bars.p_ready[1], pr[1], &bars.abort))) break;
-                    TRACE(1, 104 + j * 1000 + (k % 100) * 100000, bars.t0);
                     pr[1] ^= 1;
                     tc_fence_after();
                     issue_pv(1, vslot, j > 0);
-                    TRACE(1, 106 + j * 1000 + (k % 100) * 100000, bars.t0);
                     if (j == it.n_kv[1] - 1) tc_commit_warp(&bars.o_full[1]);
                 }
                 tc_commit_warp(&bars.kv_empty[vslot]);
                 if (next) {
                     if (j + 1 < it.n_kv[1]) {
                         issue_s(1, nslot);
-                        TRACE(1, 107 + j * 1000 + (k % 100) * 100000, bars.t0);
                         tc_commit_warp(&bars.s_full[1]);
                         if (j + 2 == it.n_kv[1]) tc_commit_warp(&bars.q_empty[1]);
                     }
@@ -537,7 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit_warp(&bars.mma_done);
         volatile int never = 0;
         mbar_wait_warp(&bars.mma_done, 0, &never);
-        CTA_LOG(2)
     } else if (warp < 4) {
         regs_dec<kRegsProducer>();  // warps 2-3: no role, registers go to the softmax warps
     } else {
@@ -553,7 +500,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = smem_u32(smem + L::kStageOff + (warp - 4) * L::kStageBytes);
         uint32_t sp = 0, o_uses = 0;
         bool ok = true;
-        const bool tr = lane == 0 && (quarter == 0);
         for (int k = 0; ok; ++k) {
             int n, lim;
             {
@@ -570,9 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m_run = -INFINITY, l = 0.f;
 
             for (int j = 0; j < n; ++j) {
-                if (tr) TRACE(2 + x, 200 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
                 if (!(ok = mbar_wait_warp<32>(&bars.s_full[x], sp, &bars.abort))) break;
-                if (tr) TRACE(2 + x, 201 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
                 sp ^= 1;
                 tc_fence_after();
                 uint32_t s[128];
@@ -582,7 +526,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     #pragma unroll
                 for (int c = 0; c < 4; ++c) reg_fence32(s + c * 32);
 
-                if (tr) TRACE(2 + x, 202 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
                 // This row sees columns [0, t) of the tile.  On a tile that crosses
                 // the causal diagonal or the padding edge, each warp sorts its
                 // 32-column chunks into seen by all its rows, hidden from all of
@@ -648,7 +591,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (tr) TRACE(2 + x, 203 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
                 const float negm = m_run == -INFINITY ? 0.f : -m_run;
                 const uint64_t sl2x2 = f2_pack(sl2, sl2), negmx2 = f2_pack(negm, negm);
                 uint64_t l4[4] = {0, 0, 0, 0};  // packed partial row sums
@@ -696,11 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t l2 = fadd2(fadd2(l4[0], l4[1]), fadd2(l4[2], l4[3]));
                     l += f2_lo(l2) + f2_hi(l2);
                 }
-                if (tr) TRACE(2 + x, 204 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&bars.p_ready[x]);
-                if (tr) TRACE(2 + x, 205 + x * 10 + j * 1000 + (k % 100) * 100000, bars.t0);
             }
 
 
@@ -708,7 +648,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // through its own buffer (64 columns per pass, 128-byte swizzled
             // rows) so that each global store instruction writes four whole
             // 128-byte row segments.
-            if (tr) TRACE(2 + x, 290 + x + (k % 100) * 100000, bars.t0);
             bool have_o = n > 0 && ok;
             if (have_o) {
                 have_o = mbar_wait_warp(&bars.o_full[x], o_uses & 1, &bars.abort);
@@ -764,13 +703,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(obh + static_cast<size_t>(row) * D + c * 64 + ch * 8) = v;
                 }
             }
-            if (tr) TRACE(2 + x, 299 + (k % 100) * 100000, bars.t0);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) { CTA_LOG(3) }
     if (warp == 1) {
         tc_fence_after();
         __syncwarp();
@@ -784,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
             atomicExch(sched, 0u);
             atomicExch(sched + 1, 0u);
+            atomicExch(sched + 2, 0u);
             __threadfence();
         }
     }
@@ -796,15 +734,21 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_sched_mutex;
 unsigned int *g_sched_base[kMaxDevices];
-std::atomic<unsigned int> g_sched_turn{0};
+std::atomic<unsigned int> g_sched_turn{0}, g_graph_turn{0}, g_epoch{0};
 
-// Work counters for one launch: a slot of g_sched, taken round-robin, so that
-// launches running at the same time on other streams count separately.
-cudaError_t sched_slot(unsigned int **out) {
+// Work counters for one launch: a slot of g_sched and a non-zero epoch.
+// Direct launches take the first kSchedSlots slots in turn, so launches
+// running at the same time on other streams count separately; a launch being
+// captured into a CUDA graph (which keeps its slot for every replay) takes
+// the next of the kGraphSlots reserved for captures.
+cudaError_t sched_slot(cudaStream_t stream, unsigned int **out, unsigned int *epoch) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return e;
     unsigned int *base;
     {
         std::lock_guard<std::mutex> lock(g_sched_mutex);
@@ -816,7 +760,15 @@ cudaError_t sched_slot(unsigned int **out) {
         }
         base = g_sched_base[dev];
     }
-    *out = base + 2 * (g_sched_turn.fetch_add(1u) % kSchedSlots);
+    const unsigned int slot = cap == cudaStreamCaptureStatusNone
+                                  ? g_sched_turn.fetch_add(1u) % kSchedSlots
+                                  : kSchedSlots + g_graph_turn.fetch_add(1u) % kGraphSlots;
+    *out = base + 4 * slot;
+    unsigned int ep;
+    do {
+        ep = g_epoch.fetch_add(1u) + 1u;
+    } while (ep == 0u);
+    *epoch = ep;
     return cudaSuccess;
 }
 
@@ -831,8 +783,8 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
                                          : static_cast<long long>(a.B) * a.H * n_major;
     if (n_items <= 0) return cudaSuccess;
     if (n_items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    unsigned int *sched = nullptr;
-    cudaError_t e = sched_slot(&sched);
+    unsigned int *sched = nullptr, epoch = 0;
+    cudaError_t e = sched_slot(a.stream, &sched, &epoch);
     if (e != cudaSuccess) return e;
     const long long sms = a.n_sm > 0 ? a.n_sm : 1;
     const unsigned grid = static_cast<unsigned>(n_items < sms ? n_items : sms);
@@ -879,7 +831,7 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
     e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     prefill_tc_kernel<D><<<grid, kThreads, L::kSmemBytes, a.stream>>>(
-        a, tq, tk, tv, n_major, static_cast<int>(group), static_cast<int>(front), static_cast<int>(n_items), sched);
+        a, tq, tk, tv, n_major, static_cast<int>(group), static_cast<int>(front), static_cast<int>(n_items), sched, epoch);
     return cudaGetLastError();
 }
 

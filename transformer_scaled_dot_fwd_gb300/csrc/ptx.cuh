@@ -18,8 +18,10 @@ namespace attn {
 // lasts microseconds.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
-// Device status word values (see attn_device_status).
+// Device status word values (see attn_device_status): the low byte is the
+// kind, the bits above it the site that reported it.
 constexpr int kStatusTimeout = 1;
+constexpr int kStatusSchedConflict = 2;  // two prefill launches in flight on one work counter
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -361,9 +363,13 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t x) {
     return __uint_as_float(x & 0xFFFF0000u);
 }
 
-// Report a timed-out wait through the device status word (first writer wins).
+// Report through the device status word (first writer wins).
+__device__ __forceinline__ void report_status(int *status, int where, int kind) {
+    if (status) atomicCAS(status, 0, (where << 8) | kind);
+}
+// Report a timed-out wait.
 __device__ __forceinline__ void report_timeout(int *status, int where) {
-    if (status) atomicCAS(status, 0, (where << 8) | kStatusTimeout);
+    report_status(status, where, kStatusTimeout);
 }
 
 }  // namespace attn
