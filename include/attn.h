@@ -109,7 +109,9 @@ extern "C" {
  * 1024 captured prefill calls should be alive.  A launch that finds its
  * counter in use by another launch records that in the device status word:
  * attn_device_status() then returns ATTN_ECONFLICT, and the outputs of both
- * launches are undefined.
+ * launches are undefined.  A conflict can leave the shared counter
+ * unbalanced, so that later launches on it report ATTN_ECONFLICT too: once
+ * no call is in flight on the device, attn_release() clears every counter.
  */
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
                       int Sq, int Skv, int D, float scale, int causal, const int32_t *kv_len,
@@ -349,8 +351,10 @@ ATTN_API const char *attn_last_error(void);
 
 /* Free library-owned device memory on the current device: the decode
  * workspace (with every smaller buffer it replaced) and attn_fwd_host's
- * device copies.  Not while a call that uses them is running, and not while
- * a CUDA graph that holds a decode call may still be replayed. */
+ * device copies; and clear the bf16 prefill work counters (the recovery after
+ * ATTN_ECONFLICT).  Not while any call of the library is running on the
+ * device, and not while a CUDA graph that holds a library call may still be
+ * replayed. */
 ATTN_API void attn_release(void);
 
 #ifdef __cplusplus

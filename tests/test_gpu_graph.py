@@ -119,6 +119,12 @@ def test_shared_counter_is_reported_or_harmless(gpu):
         attn.attn_device_status()
     except attn.AttnError as e:
         assert e.code == attn.ATTN_ECONFLICT, e
+        # the shared counter may be left unbalanced: with nothing in flight,
+        # attn_release clears every counter, and later launches are clean again
+        attn.attn_release()
+        for _ in range(70):
+            assert torch.equal(attn.attn_fwd(qs, ks, vs, causal=True), ref_s)
+        attn.attn_device_status()
         return
     assert torch.equal(long_out, ref_l)
     assert torch.equal(clash, ref_l)

@@ -660,6 +660,8 @@ ATTN_API void attn_release(void) {
     }
     // outside g_mutex: attn_fwd_host takes its own lock first, then g_mutex
     g_host[dev].release();
+    // work counters that a conflict (ATTN_ECONFLICT) may have left unbalanced
+    reset_prefill_counters();
 }
 
 }  // extern "C"

@@ -67,6 +67,10 @@ cudaError_t launch_prefill_f32(const FwdArgs &a);
 cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv);
 
+// Clears every work counter of the bf16 prefill kernel on the current device
+// (synchronous; no prefill launch may be in flight).
+cudaError_t reset_prefill_counters();
+
 // bf16 split-KV decode: partial kernel then combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a);
 

@@ -837,6 +837,13 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
 
 }  // namespace
 
+cudaError_t reset_prefill_counters() {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_sched);
+    if (e != cudaSuccess) return e;
+    return cudaMemset(p, 0, sizeof g_sched);
+}
+
 cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
                               const CUtensorMap &tv) {
     return a.D == 64 ? launch_t<64>(a, tq, tk, tv) : launch_t<128>(a, tq, tk, tv);
