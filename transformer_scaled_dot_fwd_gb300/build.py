@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libattn.so")
-SOURCES = ["api.cu", "prefill_tc.cu", "prefill_pair.cu", "prefill_f32.cu", "decode.cu", "decode_gqa.cu", "decode_tc.cu", "decode_f32.cu", "decode_noalloc.cu", "debug.cu"]
+SOURCES = ["api.cu", "prefill_tc.cu", "prefill_f32.cu", "decode.cu", "decode_gqa.cu", "decode_tc.cu", "decode_f32.cu", "decode_noalloc.cu", "debug.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -14,10 +14,6 @@
 #include <stdio.h>
 #include <string.h>
 
-#ifndef ATTN_PAIR_PREFILL
-#define ATTN_PAIR_PREFILL 0
-#endif
-
 namespace attn {
 namespace {
 
@@ -340,14 +336,11 @@ static int fwd_impl(const void *q, const void *k, const void *v, void *out, floa
         if (B > 65535 || H > 65535) return fail(ATTN_EINVAL, "attn_fwd: B and H must be <= 65535 for fp32");
         e = launch_prefill_f32(a);
     } else {
-        // D = 128 runs on CTA pairs, each CTA holding half of a key tile's rows
-        // (64-row boxes of K) and half of a value tile's columns
-        const bool pair = ATTN_PAIR_PREFILL && D == 128;
         CUtensorMap tq, tk, tv;
-        if ((rc = make_map(&tq, q, D, Sq, bh)) || (rc = make_map(&tk, k, D, Skv, bh_kv, pair ? 64 : 128)) ||
+        if ((rc = make_map(&tq, q, D, Sq, bh)) || (rc = make_map(&tk, k, D, Skv, bh_kv)) ||
             (rc = make_map(&tv, v, D, Skv, bh_kv)))
             return rc;
-        e = pair ? launch_prefill_pair(a, tq, tk, tv) : launch_prefill_tc(a, tq, tk, tv);
+        e = launch_prefill_tc(a, tq, tk, tv);
     }
     return e == cudaSuccess ? ATTN_OK : cuda_fail(e, "attn_fwd launch");
 }

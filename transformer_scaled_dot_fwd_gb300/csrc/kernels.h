@@ -71,19 +71,6 @@ cudaError_t launch_prefill_tc(const FwdArgs &a, const CUtensorMap &tq, const CUt
 // (synchronous; no prefill launch may be in flight).
 cudaError_t reset_prefill_counters();
 
-// The work counter slot (three unsigned ints: next item, finished units,
-// owner epoch) and a non-zero epoch for one bf16 prefill launch on `stream`:
-// direct launches rotate through 64 slots, launches being captured into a CUDA
-// graph take one of 1024 further slots.
-cudaError_t sched_slot(cudaStream_t stream, unsigned int **slot, unsigned int *epoch);
-
-// bf16 prefill for D = 128 on CTA pairs (tcgen05 cta_group::2): tq views Q as
-// (D, Sq, B*H) with 64 x 128 x 1 boxes, tk views K as (D, Skv, B*H_kv) with
-// 64 x 64 x 1 boxes, tv views V as (D, Skv, B*H_kv) with 64 x 128 x 1 boxes
-// (128-byte swizzle).
-cudaError_t launch_prefill_pair(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,
-                                const CUtensorMap &tv);
-
 // bf16 split-KV decode: partial kernel then combine kernel.
 cudaError_t launch_decode(const DecodeArgs &a);
 

@@ -1,5 +1,4 @@
-// Work items and their order, shared by the two bf16 prefill kernels
-// (prefill_tc.cu: one CTA per item; prefill_pair.cu: a CTA pair per item).
+// Work items of the bf16 prefill kernel (prefill_tc.cu) and their order.
 //
 // A work item is two 128-row query tiles that read the same key/value head.
 // Items are numbered in blocks of heads whose keys and values fit in part of

@@ -633,8 +633,6 @@ std::mutex g_sched_mutex;
 unsigned int *g_sched_base[kMaxDevices];
 std::atomic<unsigned int> g_sched_turn{0}, g_graph_turn{0}, g_epoch{0};
 
-}  // namespace
-
 // Work counters for one launch: a slot of g_sched and a non-zero epoch.
 // Direct launches take the first kSchedSlots slots in turn, so launches
 // running at the same time on other streams count separately; a launch being
@@ -670,8 +668,6 @@ cudaError_t sched_slot(cudaStream_t stream, unsigned int **out, unsigned int *ep
     *epoch = ep;
     return cudaSuccess;
 }
-
-namespace {
 
 template <int D>
 cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap &tk,

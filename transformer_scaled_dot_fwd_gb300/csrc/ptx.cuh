@@ -311,165 +311,6 @@ __device__ __forceinline__ void reg_fence32(uint32_t *r) {
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
 }
 
-// ---------------------------------------------------------------- CTA pairs (clusters of two)
-//
-// A CTA pair runs tcgen05 MMAs with .cta_group::2: one thread of the even CTA
-// issues each MMA, whose A rows, B halves and accumulator lanes live at the
-// same shared-memory and TMEM addresses in both CTAs.  Barriers that the
-// other CTA arrives on (remote arrivals, commits, TMA completions) are waited
-// on with acquire at cluster scope.
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Address of `p` (a shared variable of this CTA) in the shared memory of
-// cluster CTA `rank`, in the shared::cluster window.
-__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-    return r;
-}
-
-// All threads of both CTAs.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-
-// Arrive without release semantics: for hand-offs whose data is already
-// complete before the arrive is issued (TMEM stores after tcgen05.wait::st,
-// TMEM loads after tcgen05.wait::ld, plain loads into registers), so that no
-// cluster-scope fence is paid.
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr_, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr_), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
-        : "memory");
-    return ok != 0;
-}
-
-// Non-blocking test of a phase (acquire, cluster scope).
-__device__ __forceinline__ bool mbar_test_wait_cl(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// mbar_wait / mbar_wait_warp with acquire at cluster scope.
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                             long long limit = kWaitLimitCycles) {
-    if (mbar_try_wait_cl(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait_cl(bar, parity)) return true;
-        if (*abort) return false;
-        if (clock64() - t0 > limit) {
-            *abort = 1;
-            return false;
-        }
-    }
-}
-
-template <int kSleepNs = 0>
-__device__ __forceinline__ bool mbar_wait_warp_cl(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    const long long t0 = clock64();
-    for (;;) {
-        const bool ok = mbar_try_wait_cl(bar, parity);
-        if (__all_sync(0xffffffffu, ok)) return true;
-        if constexpr (kSleepNs > 0) __nanosleep(kSleepNs);
-        int give_up = 0;
-        if (lane_id() == 0) {
-            give_up = *abort != 0;
-            if (!give_up && clock64() - t0 > kWaitLimitCycles) {
-                *abort = 1;
-                give_up = 1;
-            }
-        }
-        if (__shfl_sync(0xffffffffu, give_up, 0)) return false;
-    }
-}
-
-// 3-D tiled TMA load into this CTA's shared memory that completes on a
-// barrier of either CTA of the pair (cluster address).
-__device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *map, uint32_t cluster_bar,
-                                                 int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// TMEM allocation for a pair: one warp of each CTA executes these together.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// Pair MMAs (M = 256: 128 accumulator lanes in each CTA), issued warp-wide by
-// the even CTA with one elected lane, as mma_ss_warp / mma_ts_warp.
-__device__ __forceinline__ void mma_ss_pair_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_ts_pair_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                 uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on a barrier (cluster address, either CTA) once every pair MMA the
-// elected thread issued so far has completed.
-__device__ __forceinline__ void tc_commit_pair_warp(uint32_t cluster_bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
-            cluster_bar)
-        : "memory");
-}
-
 // ---------------------------------------------------------------- registers
 
 // Move this warpgroup's register budget down / up (all four warps execute it).
