@@ -201,9 +201,17 @@ class ClockSampler:
 
 def time_steps(fn, steps, stream, flush):
     """Run fn() `steps` times; CUDA events on `stream` around each call, L2
-    flushed between calls outside the events.  Returns per-step ms."""
+    flushed between calls outside the events.  Returns per-step ms.
+
+    torch creates a CUDA event at its first record(); every event is recorded
+    once before the loop, so that no event is created between a step's flush
+    and its call (from an idle device that host work would otherwise show up
+    as a gap inside the first timed step)."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in starts + ends:
+        e.record(stream)
+    torch.cuda.synchronize()
     for s in range(steps):
         flush()
         starts[s].record(stream)
@@ -453,14 +461,15 @@ def run_ours(args):
     def step():
         attn.attn_fwd(q, k, v, out=out, scale=w.softmax_scale, causal=w.causal, kv_len=kv_len)
 
+    # the clock sampler starts first (its first sample can take seconds), so
+    # that the warm-up steps run right before the timed ones on a busy device
+    sampler = ClockSampler(local)
+    sampler.start()
     for _ in range(args.warmup):
         step()
     attn.attn_device_status()
-    torch.cuda.synchronize()
-    sampler = ClockSampler(local)
     barrier(dist, device)
     torch.cuda.synchronize()
-    sampler.start()
     wall0, tw0 = time.perf_counter(), time.time()
     ms = time_steps(step, args.steps, stream, flush)
     torch.cuda.synchronize()
