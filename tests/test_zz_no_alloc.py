@@ -5,18 +5,21 @@ front, or cannot afford the device synchronisation an allocation may cause).
 It is called through the C ABI with raw device pointers and compared with the
 regular attn_decode on the same inputs, on two calls in a row with different
 sizes (the second call must not be disturbed by what the first left in the
-library's fixed scratch).  This file is named to be collected last.
+library's fixed scratch), and both are held to the fp64 oracle as well.  This
+file is named to be collected last.
 """
 from __future__ import annotations
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import transformer_scaled_dot_fwd_gb300 as attn
 from transformer_scaled_dot_fwd_gb300 import workloads as wl
-from helpers import BF16_MAX, BF16_MEAN
+from helpers import BF16_MAX, BF16_MEAN, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -52,6 +55,8 @@ def test_noalloc_matches_decode_on_two_calls(gpu):
         err = (out.float() - ref.float()).abs()
         assert torch.isfinite(out.float()).all()
         assert err.max().item() <= BF16_MAX and err.mean().item() <= BF16_MEAN
+        exact = oracle.decode(q.cpu(), kc.cpu(), vc.cpu(), kv_len=np.array(lens, np.int32))
+        assert_close(out, exact, torch.bfloat16, f"no-allocation decode B{B} H{H} Skv{Skv} D{D} vs oracle")
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(gpu):
