@@ -11,7 +11,9 @@
 // fp32 workload (B2 H4 S128) spreads over 128 CTAs.  Sixteen threads share a
 // query row, each holding every sixteenth element of q and of the output row
 // in registers; a score is a 16-way partial dot product summed with four lane
-// shuffles.  K and V tiles of 32 keys are staged in shared memory.
+// shuffles.  K and V tiles of 32 keys are staged in shared memory, double-
+// buffered: the next tile's asynchronous copies (cp.async, zero-filled past
+// the keys the CTA needs) are in flight while this tile is computed.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -27,10 +29,23 @@ constexpr int kKeys = 32;         // keys per shared-memory tile
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
+constexpr int f32_smem_bytes() { return 2 * 2 * kKeys * D * 4; }  // [stage][K, V][key][D]
+
+// 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <int D>
 __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
     constexpr int DL = D / kLanesPerRow;
-    __shared__ __align__(16) float ks[kKeys][D];
-    __shared__ __align__(16) float vs[kKeys][D];
+    extern __shared__ __align__(16) float f32_smem[];
+    // stage st: keys ks(st)[kKeys][D], values vs(st)[kKeys][D]
+    auto ks = [&](int st) { return f32_smem + (2 * st) * kKeys * D; };
+    auto vs = [&](int st) { return f32_smem + (2 * st + 1) * kKeys * D; };
 
     const int t = threadIdx.x % kLanesPerRow;
     const int r = threadIdx.x / kLanesPerRow;
@@ -64,19 +79,32 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
     const float sl2 = a.scale * kLog2e;  // scores kept in log2 units
     float m = -INFINITY, l = 0.f;
 
-    for (int j0 = 0; j0 < cta_lim; j0 += kKeys) {
-        __syncthreads();
+    // tile j0's keys and values into stage st; rows past cta_lim are zeros
+    auto load_tile = [&](int j0, int st) {
+        const uint32_t kd = static_cast<uint32_t>(__cvta_generic_to_shared(ks(st)));
+        const uint32_t vd = static_cast<uint32_t>(__cvta_generic_to_shared(vs(st)));
         for (int idx = threadIdx.x; idx < kKeys * D / 4; idx += kThreads) {
-            const int row = idx / (D / 4), c4 = idx % (D / 4);
-            float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-            if (j0 + row < cta_lim) {
-                kk = reinterpret_cast<const float4 *>(K + static_cast<size_t>(j0 + row) * D)[c4];
-                vv = reinterpret_cast<const float4 *>(V + static_cast<size_t>(j0 + row) * D)[c4];
-            }
-            reinterpret_cast<float4 *>(ks[row])[c4] = kk;
-            reinterpret_cast<float4 *>(vs[row])[c4] = vv;
+            const int row = idx / (D / 4);
+            const bool in = j0 + row < cta_lim;
+            const size_t src = static_cast<size_t>(in ? j0 + row : 0) * D + 4 * (idx % (D / 4));
+            cp_async16(kd + 16u * idx, K + src, in ? 16u : 0u);
+            cp_async16(vd + 16u * idx, V + src, in ? 16u : 0u);
+        }
+        cp_async_commit();
+    };
+    const int n_tiles = (cta_lim + kKeys - 1) / kKeys;
+    if (n_tiles > 0) load_tile(0, 0);
+    for (int tile = 0; tile < n_tiles; ++tile) {
+        const int j0 = tile * kKeys;
+        const int st = tile & 1;
+        if (tile + 1 < n_tiles) {
+            load_tile(j0 + kKeys, st ^ 1);  // its stage was last read before the previous barrier
+            cp_async_wait<1>();              // this tile's copies have landed
+        } else {
+            cp_async_wait<0>();
         }
         __syncthreads();
+        const float *kt = ks(st), *vt = vs(st);
 
         float s[kKeys];
         float mt = -INFINITY;
@@ -84,26 +112,28 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
         for (int jj = 0; jj < kKeys; ++jj) {
             float part = 0.f;
 #pragma unroll
-            for (int d = 0; d < DL; ++d) part = fmaf(q[d], ks[jj][d * kLanesPerRow + t], part);
+            for (int d = 0; d < DL; ++d) part = fmaf(q[d], kt[jj * D + d * kLanesPerRow + t], part);
 #pragma unroll
             for (int o16 = 1; o16 < kLanesPerRow; o16 <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o16);
             s[jj] = (j0 + jj < lim) ? part * sl2 : -INFINITY;
             mt = fmaxf(mt, s[jj]);
         }
         const float mn = fmaxf(m, mt);
-        if (mn == -INFINITY) continue;  // nothing visible to this row yet
-        const float corr = exp2f(m - mn);
-        l *= corr;
+        if (mn != -INFINITY) {  // else nothing is visible to this row yet
+            const float corr = ex2_approx(m - mn);  // 2^-inf = 0 on the first visible tile
+            l *= corr;
 #pragma unroll
-        for (int d = 0; d < DL; ++d) o[d] *= corr;
+            for (int d = 0; d < DL; ++d) o[d] *= corr;
 #pragma unroll
-        for (int jj = 0; jj < kKeys; ++jj) {
-            const float p = exp2f(s[jj] - mn);
-            l += p;
+            for (int jj = 0; jj < kKeys; ++jj) {
+                const float p = ex2_approx(s[jj] - mn);  // masked keys: 2^-inf = 0
+                l += p;
 #pragma unroll
-            for (int d = 0; d < DL; ++d) o[d] = fmaf(p, vs[jj][d * kLanesPerRow + t], o[d]);
+                for (int d = 0; d < DL; ++d) o[d] = fmaf(p, vt[jj * D + d * kLanesPerRow + t], o[d]);
+            }
+            m = mn;
         }
-        m = mn;
+        __syncthreads();  // every thread is done with stage st before it is refilled
     }
 
     if (i < a.Sq) {
@@ -116,15 +146,20 @@ __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
     }
 }
 
+template <int D>
+cudaError_t launch_f32_t(const FwdArgs &a) {
+    const dim3 grid((a.Sq + kRows - 1) / kRows, a.H, a.B);
+    cudaError_t e = cudaFuncSetAttribute(prefill_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         f32_smem_bytes<D>());
+    if (e != cudaSuccess) return e;
+    prefill_f32_kernel<D><<<grid, kThreads, f32_smem_bytes<D>(), a.stream>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_f32(const FwdArgs &a) {
-    dim3 grid((a.Sq + kRows - 1) / kRows, a.H, a.B);
-    if (a.D == 64)
-        prefill_f32_kernel<64><<<grid, kThreads, 0, a.stream>>>(a);
-    else
-        prefill_f32_kernel<128><<<grid, kThreads, 0, a.stream>>>(a);
-    return cudaGetLastError();
+    return a.D == 64 ? launch_f32_t<64>(a) : launch_f32_t<128>(a);
 }
 
 }  // namespace attn
