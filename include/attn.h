@@ -110,8 +110,10 @@ extern "C" {
  * counter in use by another launch records that in the device status word:
  * attn_device_status() then returns ATTN_ECONFLICT, and the outputs of both
  * launches are undefined.  A conflict can leave the shared counter
- * unbalanced, so that later launches on it report ATTN_ECONFLICT too: once
- * no call is in flight on the device, attn_release() clears every counter.
+ * unbalanced, and so can a launch that gave up on a device-side wait
+ * (ATTN_ETIMEOUT), so that later launches on it report ATTN_ECONFLICT too:
+ * once no call is in flight on the device, attn_release() clears every
+ * counter.
  */
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *out, int B, int H,
                       int Sq, int Skv, int D, float scale, int causal, const int32_t *kv_len,

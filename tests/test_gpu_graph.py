@@ -3,8 +3,8 @@
 A decode loop replays the same launches once per token, so launch overhead
 matters; a CUDA graph removes it.  After one ordinary call (which sizes the
 decode workspace), attn_fwd and attn_decode can be captured: the persistent
-prefill kernel's work counter is reset by its last CTA, so every replay
-starts from zero, and the decode partials live in the library's workspace.
+prefill kernel's work counter is reset by the CTA that draws the launch's
+last item number, so every replay starts from zero, and the decode partials live in the library's workspace.
 Replays with new data copied into the captured buffers must equal ordinary
 calls bit for bit.
 """

@@ -95,14 +95,22 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
 
-// Work counters, one slot per launch: [0] next item, [1] CTAs finished,
-// [2] epoch of the launch using the slot (0: free).  The last CTA of a launch
-// resets all three, so the next launch on the slot starts from zero without a
-// separate clearing step.  Direct launches take slots [0, kSchedSlots) in
-// turn; a launch captured into a CUDA graph gets its own slot from the
-// kGraphSlots after them, so replays never share a counter with direct
-// launches.  A CTA that finds another launch's epoch in its slot reports
-// kStatusSchedConflict: the two launches' outputs are then undefined.
+// Work counters, one slot per launch: [0] next item, [2] epoch of the launch
+// using the slot (0: free); [1] and [3] unused.  Every CTA's producer takes
+// items until it draws one past the end, so a launch draws exactly n_items +
+// gridDim.x numbers: the CTA that draws the last one resets the slot (no CTA
+// of the launch touches it after that), and the next launch on the slot
+// starts from zero without a clearing step or any atomic at the end of the
+// kernel.  Each CTA claims the slot (writes its epoch) at its start, before
+// its first draw, which is a release operation; the last drawer fences before
+// it resets the epoch, so no claim can land after the reset.  Direct launches
+// take slots [0, kSchedSlots) in turn; a launch captured into a CUDA graph
+// gets its own slot from the kGraphSlots after them, so replays never share a
+// counter with direct launches.  A CTA that finds another launch's epoch in
+// its slot reports kStatusSchedConflict: the two launches' outputs are then
+// undefined.  A launch that gave up on a wait may stop drawing early and
+// leave its slot claimed; later launches on that slot then report the
+// conflict until the counters are cleared from the host.
 __device__ unsigned int g_sched[kSchedSlots + kGraphSlots][4];
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
@@ -166,7 +174,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
+    unsigned int owner = 0u;
     if (threadIdx.x == 0) {
+        // claim the slot for this launch (the first CTA finds it free, the
+        // others this launch's epoch); the result is checked after the
+        // prologue, so the atomic's round trip overlaps it
+        owner = atomicExch(sched + 2, epoch);
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
         for (int x = 0; x < kQTiles; ++x) {
             mbar_init(&bars.q_full[x], 1);
             mbar_init(&bars.q_empty[x], 1);
@@ -185,10 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars.mma_done, 1);
         bars.abort = 0;
         fence_mbar_init();
-        // claim the slot for this launch (the first CTA finds it free, the
-        // others find this launch's epoch)
-        const unsigned int owner = atomicExch(sched + 2, epoch);
-        if (owner != 0u && owner != epoch) report_status(a.status, 0x12, kStatusSchedConflict);
     }
     if (warp == 1) {
         tmem_alloc(&bars.tmem_base, kTmemCols);
@@ -203,9 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================================================================ TMA producer
         regs_dec<kRegsProducer>();
         if (lane == 0) {
-            prefetch_tmap(&tq);
-            prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
+            if (owner != 0u && owner != epoch) report_status(a.status, 0x12, kStatusSchedConflict);
+            const unsigned int last_draw = static_cast<unsigned int>(n_items) + gridDim.x - 1u;
             uint32_t q_uses[kQTiles] = {0, 0};  // Q_x loads issued so far
             int issued = 0;                     // K/V ring loads issued so far
             bool ok = true;
@@ -215,7 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k >= kItemRing &&
                     !(ok = mbar_wait(&bars.item_empty[slot], ((k / kItemRing) - 1) & 1, &bars.abort)))
                     break;
-                const int t = static_cast<int>(atomicAdd(sched, 1u));
+                // the first draw releases this CTA's claim of the slot
+                const unsigned int drawn = k == 0 ? atomic_add_release_gpu(sched, 1u) : atomicAdd(sched, 1u);
+                if (drawn == last_draw) {  // the launch's last draw: free the slot
+                    fence_acq_rel_gpu();
+                    atomicExch(sched, 0u);
+                    atomicExch(sched + 2, 0u);
+                }
+                const int t = static_cast<int>(drawn);
                 Item it;
                 if (t < n_items) {
                     it = decode_item(t, a, n_major, group, front);
@@ -611,18 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         tmem_dealloc(tmem, kTmemCols);
     }
-    if (threadIdx.x == 0) {
-        if (bars.abort) report_timeout(a.status, 0x11);
-        // Every producer of this launch has taken its last item once all CTAs
-        // have counted themselves here: the last one resets the slot.
-        __threadfence();
-        if (atomicAdd(sched + 1, 1u) == gridDim.x - 1) {
-            atomicExch(sched, 0u);
-            atomicExch(sched + 1, 0u);
-            atomicExch(sched + 2, 0u);
-            __threadfence();
-        }
-    }
+    if (threadIdx.x == 0 && bars.abort) report_timeout(a.status, 0x11);
 }
 
 }  // namespace

@@ -363,6 +363,16 @@ __device__ __forceinline__ float bf16hi_to_f32(uint32_t x) {
     return __uint_as_float(x & 0xFFFF0000u);
 }
 
+// Work-counter increment with release semantics at GPU scope: the thread's
+// earlier memory operations are visible to any thread that observes the new
+// value (directly or through later increments) and then fences.
+__device__ __forceinline__ unsigned int atomic_add_release_gpu(unsigned int *p, unsigned int v) {
+    unsigned int old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // Report through the device status word (first writer wins).
 __device__ __forceinline__ void report_status(int *status, int where, int kind) {
     if (status) atomicCAS(status, 0, (where << 8) | kind);
