@@ -54,6 +54,7 @@ from transformer_scaled_dot_fwd_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "causal attn fwd TFLOP/s (B4 H32 S2048 D128 bf16) and % peak; decode HBM GB/s"
 L2_FLUSH_BYTES = 256 << 20   # > the 129 MB L2
+SETTLE_S = 0.01              # untimed flush + call before the timed steps (see time_steps)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -174,7 +175,7 @@ class ClockSampler:
                     float("0." + r[9].split(".")[1]) if "." in r[9] else 0.0
             except (ValueError, IndexError):
                 ts = 0.0
-            if self.window and self.window[0] - 0.05 <= ts <= self.window[1] + 0.05:
+            if self.window and self.window[0] - 0.02 <= ts <= self.window[1] + 0.02:
                 inside.append(r)
         if inside:
             rows = inside
@@ -199,9 +200,12 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- timing
 
-def time_steps(fn, steps, stream, flush):
+def time_steps(fn, steps, stream, flush, window=None):
     """Run fn() `steps` times; CUDA events on `stream` around each call, L2
-    flushed between calls outside the events.  Returns per-step ms.
+    flushed between calls outside the events (untimed flush + call first,
+    for SETTLE_S).  Returns per-step ms.  If `window` is a dict, its "t0" and
+    "t1" receive the wall-clock times (time.time()) that bracket the timed
+    steps, for the clock sampler.
 
     torch creates a CUDA event at its first record(); every event is recorded
     once before the loop, so that no event is created between a step's flush
@@ -211,13 +215,28 @@ def time_steps(fn, steps, stream, flush):
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for e in starts + ends:
         e.record(stream)
+    # untimed first: one flush + call (the flush kernel's first launch loads
+    # its module, which on a fresh machine can take a quarter of a second),
+    # then flush + call repeated for SETTLE_S, so that the timed steps do not
+    # start on a device that has just dropped to its idle clocks
+    flush()
+    fn()
     torch.cuda.synchronize()
+    t_settle = time.perf_counter()
+    while time.perf_counter() - t_settle < SETTLE_S:
+        flush()
+        fn()
+        torch.cuda.synchronize()
+    if window is not None:
+        window["t0"] = time.time()
     for s in range(steps):
         flush()
         starts[s].record(stream)
         fn()
         ends[s].record(stream)
     torch.cuda.synchronize()
+    if window is not None:
+        window["t1"] = time.time()
     return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
@@ -420,7 +439,8 @@ def config_dict(w, world):
             "global_batch": w.B * world, "seq_len": w.S,
             "parallelism": f"dp{world} (independent sequences per GPU, no collective)" if world > 1 else "single GPU",
             "l2": "flushed between steps (256 MB write), outside the timed events",
-            "timing": "CUDA events on the launching stream around each call; sum over steps; max over ranks"}
+            "timing": "CUDA events on the launching stream around each call; sum over steps; max over ranks; "
+                      "before the timed steps, untimed flush + call for 10 ms after the warm-up steps"}
 
 
 def run_ours(args):
@@ -470,11 +490,10 @@ def run_ours(args):
     attn.attn_device_status()
     barrier(dist, device)
     torch.cuda.synchronize()
-    wall0, tw0 = time.perf_counter(), time.time()
-    ms = time_steps(step, args.steps, stream, flush)
-    torch.cuda.synchronize()
-    wall, tw1 = time.perf_counter() - wall0, time.time()
-    sampler.mark(tw0, tw1)
+    window = {}
+    ms = time_steps(step, args.steps, stream, flush, window)
+    wall = window["t1"] - window["t0"]
+    sampler.mark(window["t0"], window["t1"])
     clocks = sampler.stop()
     barrier(dist, device)
     attn.attn_device_status()
@@ -518,6 +537,8 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) Q/K/V rounded to bf16)",
         "config": config_dict(w, world),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode, "configs": configs,
+        "step_ms": {"mean": avg_ms, "median": float(sorted(ms)[len(ms) // 2]), "min": float(min(ms)),
+                    "max": float(max(ms))},
         "clocks": clocks, "gpu_launches": args.steps,
         "wall_s_timed_region": wall, "kernel_source_digest": kernel_source_digest(),
         "env": run_env(device, {"prefill": w.seed, "decode": wl.DECODE.seed, "rank_offset": 1000}),
@@ -665,15 +686,18 @@ def prefill_workload_leg(name, args, attn, device, stream, flush, peaks, world, 
             "flops_nominal": nominal, "flops_effective": effective,
             "TFLOP_per_s_nominal": nominal / (avg * 1e-3) / 1e12,
             "TFLOP_per_s_effective": effective / (avg * 1e-3) / 1e12,
-            "kernel": kernel, "gpu_launches": args.steps}
+            "kernel": kernel, "gpu_launches": args.steps,
+            "step_ms": {"median": float(sorted(ms)[len(ms) // 2]), "min": float(min(ms)), "max": float(max(ms))}}
     if w.dtype == "f32":
         line["roofline"] = {"bound": "latency", "note": "16.8 MFLOP per call: too small to fill the GPU; "
                             "the figure is the time per call"}
     else:
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
         achieved = line["TFLOP_per_s_effective"]
+        peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
         line["roofline"] = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                            "frac": achieved / peak,
+                            "frac": achieved / peak, "peak_sustained": peak_sus,
+                            "frac_sustained": achieved / peak_sus,
                             "traffic": profiled_traffic(PROFILE_SUMMARIES[name], "prefill_tc.cu"),
                             "kernel": kernel, "algorithmic_flops_per_launch": effective}
     return line, (q, k, v, kv_len)
