@@ -45,6 +45,7 @@ struct __align__(128) DecodeSmem {
 template <int D>
 __global__ void __launch_bounds__(kThreads) decode_partial_kernel(DecodeArgs a) {
     griddep_launch_dependents();
+    griddep_wait();  // launched back to back: the previous kernel's writes are visible
     extern __shared__ __align__(128) uint8_t smem_raw[];
     DecodeSmem<D> &sm = *reinterpret_cast<DecodeSmem<D> *>(smem_raw);
 
@@ -332,10 +333,10 @@ cudaError_t launch_decode_t(const DecodeArgs &a) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const long long blocks = static_cast<long long>(a.B) * a.H * a.n_split;
-    if (a.Skv > 0)
-        decode_partial_kernel<D><<<static_cast<unsigned>(blocks), kThreads, smem, a.stream>>>(a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (a.Skv > 0) {
+        e = launch_pdl(decode_partial_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem, a.stream, a);
+        if (e != cudaSuccess) return e;
+    }
     return launch_decode_combine(a);
 }
 

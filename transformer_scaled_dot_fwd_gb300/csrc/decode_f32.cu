@@ -26,6 +26,8 @@ constexpr float kF32Log2e = 1.4426950408889634f;
 
 template <int D>
 __global__ void __launch_bounds__(kF32Threads) decode_f32_partial_kernel(DecodeArgs a) {
+    griddep_launch_dependents();  // the combine may be placed once every CTA has started
+    griddep_wait();               // launched back to back: the previous kernel's writes are visible
     __shared__ float s[kDecodeMaxChunk];  // scores, then probabilities, of the chunk
     __shared__ float red[kF32Warps][D];
     __shared__ float wred[kF32Warps];
@@ -140,6 +142,7 @@ __global__ void __launch_bounds__(kF32Threads) decode_f32_partial_kernel(DecodeA
 
 template <int D>
 __global__ void __launch_bounds__(D) decode_f32_combine_kernel(DecodeArgs a) {
+    griddep_wait();  // the partial kernel's results
     const int bh = blockIdx.x;
     const int d = threadIdx.x;
     const int b = bh / a.H;
@@ -168,12 +171,11 @@ template <int D>
 cudaError_t launch_f32_t(const DecodeArgs &a) {
     if (a.Skv > 0) {
         const long long blocks = static_cast<long long>(a.B) * a.H * a.n_split;
-        decode_f32_partial_kernel<D><<<static_cast<unsigned>(blocks), kF32Threads, 0, a.stream>>>(a);
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e = launch_pdl(decode_f32_partial_kernel<D>, dim3(static_cast<unsigned>(blocks)),
+                                         dim3(kF32Threads), 0, a.stream, a);
         if (e != cudaSuccess) return e;
     }
-    decode_f32_combine_kernel<D><<<a.B * a.H, D, 0, a.stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_f32_combine_kernel<D>, dim3(static_cast<unsigned>(a.B * a.H)), dim3(D), 0, a.stream, a);
 }
 
 }  // namespace

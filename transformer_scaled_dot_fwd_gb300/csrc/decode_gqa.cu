@@ -49,6 +49,7 @@ struct __align__(128) GqaSmem {
 template <int D, int GT>
 __global__ void __launch_bounds__(kThreads) decode_gqa_partial_kernel(DecodeArgs a, int n_sub) {
     griddep_launch_dependents();
+    griddep_wait();  // launched back to back: the previous kernel's writes are visible
     extern __shared__ __align__(128) uint8_t smem_raw[];
     GqaSmem<D, GT> &sm = *reinterpret_cast<GqaSmem<D, GT> *>(smem_raw);
 
@@ -309,10 +310,11 @@ cudaError_t launch_gqa_t(const DecodeArgs &a) {
     const int G = a.H / a.H_kv;
     const int n_sub = (G + GT - 1) / GT;
     const long long blocks = static_cast<long long>(a.B) * a.H_kv * n_sub * a.n_split;
-    if (a.Skv > 0)
-        decode_gqa_partial_kernel<D, GT><<<static_cast<unsigned>(blocks), kThreads, smem, a.stream>>>(a, n_sub);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (a.Skv > 0) {
+        e = launch_pdl(decode_gqa_partial_kernel<D, GT>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), smem,
+                       a.stream, a, n_sub);
+        if (e != cudaSuccess) return e;
+    }
     return launch_decode_combine(a);
 }
 

@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kTcThreads, kTcMinBlocks)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tq,
                      const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv) {
     griddep_launch_dependents();  // the combine may be placed once every CTA has started
+    griddep_wait();               // launched back to back: the previous kernel's writes are visible
     using L = TcLayout<D>;
     const int c = blockIdx.x;   // chunk of keys
     const int bk = blockIdx.y;  // b * H_kv + h_kv
@@ -329,8 +330,7 @@ cudaError_t launch_tc_t(const DecodeArgs &a, const CUtensorMap &tq, const CUtens
     if (e != cudaSuccess) return e;
     if (a.Skv > 0) {
         const dim3 grid(static_cast<unsigned>(a.n_split), static_cast<unsigned>(a.B * a.H_kv));
-        decode_tc_kernel<D><<<grid, kTcThreads, L::kSmemBytes, a.stream>>>(a, tq, tk, tv);
-        e = cudaGetLastError();
+        e = launch_pdl(decode_tc_kernel<D>, grid, dim3(kTcThreads), L::kSmemBytes, a.stream, a, tq, tk, tv);
         if (e != cudaSuccess) return e;
     }
     return launch_decode_combine(a);

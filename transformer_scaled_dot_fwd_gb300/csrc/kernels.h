@@ -8,6 +8,26 @@
 
 namespace attn {
 
+// Launch with programmatic stream serialisation: the kernel may be placed
+// while the previous kernel in the stream finishes, and waits for it
+// (griddepcontrol.wait) before it reads its inputs or writes anything, so
+// back-to-back launches do not pay the full launch gap.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 struct FwdArgs {
     const void *q, *k, *v;  // (B, H, Sq|Skv, D), device
     void *out;              // (B, H, Sq, D), device

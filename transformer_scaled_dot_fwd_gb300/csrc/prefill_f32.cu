@@ -42,6 +42,8 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 template <int D>
 __global__ void __launch_bounds__(kThreads) prefill_f32_kernel(FwdArgs a) {
     constexpr int DL = D / kLanesPerRow;
+    griddep_launch_dependents();
+    griddep_wait();  // launched back to back: the previous kernel's writes are visible
     extern __shared__ __align__(16) float f32_smem[];
     // stage st: keys ks(st)[kKeys][D], values vs(st)[kKeys][D]
     auto ks = [&](int st) { return f32_smem + (2 * st) * kKeys * D; };
@@ -152,8 +154,7 @@ cudaError_t launch_f32_t(const FwdArgs &a) {
     cudaError_t e = cudaFuncSetAttribute(prefill_f32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          f32_smem_bytes<D>());
     if (e != cudaSuccess) return e;
-    prefill_f32_kernel<D><<<grid, kThreads, f32_smem_bytes<D>(), a.stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(prefill_f32_kernel<D>, grid, dim3(kThreads), f32_smem_bytes<D>(), a.stream, a);
 }
 
 }  // namespace

@@ -210,6 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
+    // Launched with programmatic stream serialisation: the prologue above may
+    // overlap the previous kernel in the stream; nothing it wrote is read (and
+    // nothing is written) before that kernel has finished.  The next kernel
+    // may be placed as soon as every CTA of this one has started.
+    griddep_launch_dependents();
+    griddep_wait();
 
     if (warp == 0) {
         // ================================================================ TMA producer
@@ -690,9 +696,10 @@ cudaError_t launch_t(const FwdArgs &a, const CUtensorMap &tq, const CUtensorMap 
     const unsigned grid = static_cast<unsigned>(plan.n_items < sms ? plan.n_items : sms);
     e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
-    prefill_tc_kernel<D><<<grid, kThreads, L::kSmemBytes, a.stream>>>(
-        a, tq, tk, tv, plan.n_major, plan.group, plan.front, plan.n_items, sched, epoch);
-    return cudaGetLastError();
+    // programmatic dependent launch: back to back with the previous kernel,
+    // the launch and the prologue overlap its end (griddep_wait in the kernel)
+    return launch_pdl(prefill_tc_kernel<D>, dim3(grid), dim3(kThreads), L::kSmemBytes, a.stream, a, tq, tk, tv,
+                      plan.n_major, plan.group, plan.front, plan.n_items, sched, epoch);
 }
 
 }  // namespace
