@@ -27,6 +27,11 @@
  * Streams.  `stream` is a cudaStream_t (NULL = the legacy default stream).
  *           Calls are asynchronous: they enqueue work and return.  Argument
  *           errors are detected on the host before anything is enqueued.
+ *           Kernels are launched with programmatic stream serialisation
+ *           (programmatic dependent launch): one may be placed while the
+ *           previous kernel in the stream finishes, but it reads no input
+ *           and writes nothing before that kernel has completed, so stream
+ *           order holds as for an ordinary launch.
  * dtype.    ATTN_BF16: bfloat16 inputs and output, fp32 accumulation and
  *           softmax statistics, output rounded to nearest even.
  *           ATTN_F32: float32 everywhere (no TF32).  Output dtype = input dtype.
