@@ -89,3 +89,40 @@ def test_overwrite_after_read(gpu):
         torch.cuda.synchronize()
         attn.attn_device_status()
         assert torch.equal(out, ref)
+
+
+def test_captured_chain_replays(gpu):
+    """A chain of dependent calls captured in one CUDA graph (the programmatic
+    launches become programmatic edges) replays to the eager chain's result."""
+    B, H, S, D = 2, 8, 900, 128
+    q, k, v = wl.random_tensors((B, H, S, D), 80)
+    qd = wl.random_tensors((B, H, D), 81, count=1)[0]
+    kl = torch.tensor([900, 333], dtype=torch.int32, device="cuda")
+    x1, x2, x3 = (torch.empty_like(q) for _ in range(3))
+    d1, d2 = torch.empty_like(qd), torch.empty_like(qd)
+
+    def chain():
+        attn.attn_fwd(q, k, v, out=x1, causal=True)
+        attn.attn_fwd(x1, k, v, out=x2, causal=True)          # reads x1
+        attn.attn_fwd(x2, x1, v, out=x3, causal=True)         # reads x2 and x1
+        attn.attn_decode(qd, x3, v, out=d1, kv_len=kl)        # the cache is x3
+        attn.attn_decode(d1, x3, x2, out=d2, kv_len=kl)       # reads d1
+
+    chain()  # sizes the decode workspace
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for seed in (90, 95):
+        for t, s in ((q, seed), (k, seed + 1), (v, seed + 2), (qd, seed + 3)):
+            t.copy_(wl.random_tensors(tuple(t.shape), s, count=1)[0])
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (x1, x2, x3, d1, d2)]
+        for t in (x1, x2, x3, d1, d2):
+            t.fill_(float("nan"))
+        chain()
+        torch.cuda.synchronize()
+        attn.attn_device_status()
+        for a, b in zip(got, (x1, x2, x3, d1, d2)):
+            assert torch.equal(a, b)
